@@ -1,0 +1,25 @@
+"""Shared pytest configuration.
+
+Markers:
+  gpu  -- needs a CUDA device (a GB300, sm_103a); runs the product kernels
+          through the C ABI and compares them with the CPU oracle.
+Tests without the marker run on any host: the oracle against its pins, the
+host-side logic, and the C-ABI library's exported symbols.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
+
+
+@pytest.fixture(scope="session")
+def golden_dir():
+    return os.path.join(ROOT, "tests", "golden")
