@@ -1,0 +1,509 @@
+"""Benchmark of the MX hot path on GB300.
+
+Headline workload (one JSON line on rank 0): MXFP8 quantize + dequantize of a
+bf16 4096 x 4096 activation tensor (blocks of 32 along the last axis, the
+seeded synthetic workload with heavy tails, zero / tiny / subnormal blocks and
+64 NaN-scale blocks).  One step = mx_quantize (bf16 -> E4M3 codes + E8M0
+scales) then mx_dequantize (-> f32).  value = algorithmic bytes of both calls
+per step / step time, summed over ranks.
+
+The same line carries the block_matmul workloads (decode 16x14336x4096
+E4M3 x E2M1 with its on-the-fly activation quantize, square 8192^3 MXFP8, and
+prefill 8192x28672x8192 MXFP4 with its activation quantize) under
+``block_matmul``, the dominant kernel's roofline, an end-to-end number through
+host buffers, and the CPU oracle's throughput on a bounded sample.
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
+graphs between CUDA events on the launching stream, with a device
+synchronize (and a barrier across ranks) on both sides; the maximum time over
+ranks is used.  Inputs rotate over enough buffer sets that one rotation
+exceeds 3x the L2 size, so no step finds its inputs in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  (N > 1: launch with torch.distributed.run, one rank per GPU; the workload is
+  replicated per GPU -- weak scaling, no data-path collective.)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MX quantize GB/s (% HBM peak); block_matmul TFLOPS (% dense MX tensor peak)"
+HEADLINE = "mxfp8_act_4096: bf16 4096x4096 -> MXFP8 (E4M3FN + E8M0) quantize, then dequantize -> f32"
+NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}  # dense tensor rates relative to bf16
+
+
+# ------------------------------------------------------------------ plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job rate: every rank processed `units_per_rank`; the job took the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def l2_bytes() -> int:
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 126 * 2 ** 20
+
+
+def sets_for(bytes_per_step: int) -> int:
+    return max(2, math.ceil(3 * l2_bytes() / bytes_per_step))
+
+
+def timed_graph_steps(step_fn, nsets: int, steps: int, warmup: int, world: int):
+    """Run `warmup` eager steps, then exactly `steps` steps from CUDA graphs,
+    timed with events on the capturing stream.  Returns (seconds, launches per step).
+    step_fn(i) issues the work of step i on the current stream."""
+    for i in range(warmup):
+        step_fn(i % nsets)
+    torch.cuda.synchronize()
+    per_graph = max(nsets, min(steps, 256) // nsets * nsets)
+    stream = torch.cuda.Stream()
+    graphs = []
+    counts = []
+    remaining = steps
+    with torch.cuda.stream(stream):
+        while remaining > 0 and len(graphs) < 2:
+            n = per_graph if remaining >= per_graph else remaining
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step_fn(i % nsets)
+            reps = remaining // n if len(graphs) == 0 else 1
+            graphs.append(g)
+            counts.append(reps)
+            remaining -= reps * n
+        assert remaining == 0
+        torch.cuda.synchronize()
+        graphs[0].replay()  # upload / first-replay cost kept out of the timed region
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for g, reps in zip(graphs, counts):
+            for _ in range(reps):
+                g.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end) / 1e3
+
+
+# ------------------------------------------------------------- workloads
+
+def headline_bytes(rows, cols):
+    """Algorithmic bytes of quantize (bf16 in, E4M3 codes + scales out) and of
+    dequantize (codes + scales in, f32 out)."""
+    n = rows * cols
+    q = 2 * n + n + n // 32
+    d = n + n // 32 + 4 * n
+    return q, d
+
+
+def bench_headline(mx, steps, warmup, world, peaks, device_index):
+    w = workloads.make(2)
+    rows, cols = w["rows"], w["cols"]
+    qb, db = headline_bytes(rows, cols)
+    nsets = sets_for(qb + db)
+    x0 = w["x"].cuda()
+    sets = []
+    for i in range(nsets):
+        sets.append({"x": x0.clone(), "codes": mx.alloc_codes(rows, cols, mx.E4M3FN),
+                     "scales": mx.alloc_scales(rows, cols), "y": torch.empty(rows, cols, device="cuda")})
+    nan_blocks = torch.from_numpy(w["nan_blocks"]).cuda()
+
+    def step(i):
+        s = sets[i]
+        mx.mx_quantize(s["x"], mx.E4M3FN, s["codes"], s["scales"])
+        mx.mx_dequantize(s["codes"], s["scales"], rows, cols, mx.E4M3FN, s["y"])
+
+    def deq_only(i):
+        s = sets[i]
+        mx.mx_dequantize(s["codes"], s["scales"], rows, cols, mx.E4M3FN, s["y"])
+
+    def q_only(i):
+        s = sets[i]
+        mx.mx_quantize(s["x"], mx.E4M3FN, s["codes"], s["scales"])
+
+    # correctness of what is timed: the 64 NaN-scale blocks poison their blocks
+    step(0)
+    s0 = sets[0]
+    s0["scales"][nan_blocks] = 0xFF
+    mx.mx_dequantize(s0["codes"], s0["scales"], rows, cols, mx.E4M3FN, s0["y"])
+    mx.mx_device_status()
+    assert int(torch.isnan(s0["y"].view(-1, 32)).all(dim=1).sum()) >= 64
+
+    with ClockSampler(device_index) as clk:
+        sec = timed_graph_steps(step, nsets, steps, warmup, world)
+    sec = max_over_ranks(sec, world)
+    value = job_throughput((qb + db) * steps, world, sec) / 1e9
+    # per-kernel timing for the roofline (same stream, same rotation)
+    k_steps = max(steps, 200)
+    sec_d = max_over_ranks(timed_graph_steps(deq_only, nsets, k_steps, 3, world), world)
+    sec_q = max_over_ranks(timed_graph_steps(q_only, nsets, k_steps, 3, world), world)
+    deq_gbs = db * k_steps / sec_d / 1e9
+    q_gbs = qb * k_steps / sec_q / 1e9
+    mx.mx_device_status()
+    return {
+        "value": value, "ms_per_step": sec / steps * 1e3, "clocks": clk.summary(), "nsets": nsets,
+        "launches": 2 * steps,
+        "quantize": {"gbs": q_gbs, "us": sec_q / k_steps * 1e6, "bytes": qb, "frac": q_gbs / peaks["hbm_gbs"]},
+        "dequantize": {"gbs": deq_gbs, "us": sec_d / k_steps * 1e6, "bytes": db, "frac": deq_gbs / peaks["hbm_gbs"]},
+        "dominant": "dequantize" if sec_d >= sec_q else "quantize",
+        "x_host": w["x"], "rows": rows, "cols": cols, "bytes": qb + db,
+    }
+
+
+def bench_e2e(mx, hl, steps, world):
+    """Same metric through the public API with host buffers: per step, copy the
+    bf16 input from pinned host memory, quantize, dequantize, copy the f32
+    result back to pinned host memory."""
+    rows, cols = hl["rows"], hl["cols"]
+    x_host = hl["x_host"].pin_memory()
+    y_host = torch.empty(rows, cols, dtype=torch.float32).pin_memory()
+    x = torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(rows, cols, device="cuda")
+    codes, scales = mx.alloc_codes(rows, cols, mx.E4M3FN), mx.alloc_scales(rows, cols)
+    n = max(3, min(steps, 100))
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        x.copy_(x_host, non_blocking=True)
+        mx.mx_quantize(x, mx.E4M3FN, codes, scales)
+        mx.mx_dequantize(codes, scales, rows, cols, mx.E4M3FN, y)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(n):
+        x.copy_(x_host, non_blocking=True)
+        mx.mx_quantize(x, mx.E4M3FN, codes, scales)
+        mx.mx_dequantize(codes, scales, rows, cols, mx.E4M3FN, y)
+        y_host.copy_(y, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    mx.mx_device_status()
+    return {"value": job_throughput(hl["bytes"] * n, world, sec) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": rows * cols * 2, "d2h_bytes_per_step": rows * cols * 4, "steps": n}
+
+
+def bench_gemm(mx, cfg, steps, warmup, world, peaks):
+    """block_matmul workloads.  Weights are quantized before timing; the step
+    includes the activation quantize where the workload quantizes on the fly."""
+    w = workloads.make(cfg)
+    M, N, K = w["M"], w["N"], w["K"]
+    if cfg == 3:
+        fa, fb, a_key, b_key, quant_a, kind = mx.E4M3FN, mx.E2M1, "A", "W", True, "fp8"
+    elif cfg == 4:
+        fa, fb, a_key, b_key, quant_a, kind = mx.E4M3FN, mx.E4M3FN, "A", "Bt", False, "fp8"
+    else:
+        fa, fb, a_key, b_key, quant_a, kind = mx.E2M1, mx.E2M1, "A", "W", True, "fp4"
+    L = mx.SCALES_MMA
+    A = torch.as_tensor(w[a_key]).cuda()
+    B = torch.as_tensor(w[b_key]).cuda()
+    C0 = torch.from_numpy(w["C0"]).cuda()
+    bc, bs = mx.alloc_codes(N, K, fb), mx.alloc_scales(N, K, L)
+    mx.mx_quantize(B, fb, bc, bs, L)
+    del B
+    a_bytes_in = A.numel() * A.element_size()
+    ca_b, sa_b = mx.mx_codes_bytes(fa, M, K), mx.mx_scales_bytes(L, M, K)
+    gemm_bytes = ca_b + sa_b + mx.mx_codes_bytes(fb, N, K) + mx.mx_scales_bytes(L, N, K) + 8 * M * N
+    step_bytes = gemm_bytes + (a_bytes_in + ca_b + sa_b if quant_a else 0)
+    nsets = sets_for(step_bytes) if step_bytes < 3 * l2_bytes() else 1
+    # rotate only what fits; the weight (B) is shared, A and C rotate
+    sets = []
+    for i in range(nsets):
+        ac, as_ = mx.alloc_codes(M, K, fa), mx.alloc_scales(M, K, L)
+        if not quant_a:
+            mx.mx_quantize(A, fa, ac, as_, L)
+        sets.append({"A": A.clone() if (quant_a and i) else A, "ac": ac, "as": as_, "C": C0.clone()})
+    if nsets > 1 and cfg == 3:
+        # the decode weight (29 MB) would stay in L2 across steps: rotate it too
+        for i, s in enumerate(sets):
+            if i == 0:
+                s["bc"], s["bs"] = bc, bs
+            else:
+                s["bc"], s["bs"] = bc.clone(), bs.clone()
+    for s in sets:
+        s.setdefault("bc", bc)
+        s.setdefault("bs", bs)
+
+    def step(i):
+        s = sets[i]
+        if quant_a:
+            mx.mx_quantize(s["A"], fa, s["ac"], s["as"], L)
+        mx.mx_block_matmul(s["ac"], s["as"], fa, s["bc"], s["bs"], fb, M, N, K, s["C"], L)
+
+    def gemm_only(i):
+        s = sets[i]
+        mx.mx_block_matmul(s["ac"], s["as"], fa, s["bc"], s["bs"], fb, M, N, K, s["C"], L)
+
+    step(0)
+    mx.mx_device_status()
+    sec = max_over_ranks(timed_graph_steps(step, nsets, steps, warmup, world), world)
+    sec_g = max_over_ranks(timed_graph_steps(gemm_only, nsets, steps, 3, world), world)
+    mx.mx_device_status()
+    flops = 2.0 * M * N * K
+    tf_step = job_throughput(flops * steps, world, sec) / 1e12
+    tf_gemm = flops * steps / sec_g / 1e12
+    peak_tf = peaks["bf16_tflops"] * NOMINAL_RATIO[kind]
+    gbs_gemm = gemm_bytes * steps / sec_g / 1e9
+    out = {"workload": workloads.NAMES[cfg], "M": M, "N": N, "K": K, "formats": {
+        3: "E4M3 x E2M1", 4: "E4M3 x E4M3", 5: "E2M1 x E2M1"}[cfg],
+        "step": "quantize A + block_matmul" if quant_a else "block_matmul",
+        "tflops_step": tf_step, "us_per_step": sec / steps * 1e6,
+        "tflops_gemm": tf_gemm, "us_gemm": sec_g / steps * 1e6,
+        "tensor_peak_tflops": peak_tf, "tensor_frac": tf_gemm / peak_tf,
+        "gemm_gbs": gbs_gemm, "hbm_frac": gbs_gemm / peaks["hbm_gbs"], "gemm_bytes": gemm_bytes,
+        "launches_per_step": 2 if quant_a else 1, "nsets": nsets}
+    del sets, A, C0, bc, bs
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------- CPU baseline
+
+def oracle_step_rate(rows_sample: int, x_full: torch.Tensor, reps: int = 1):
+    """Oracle quantize + dequantize of `rows_sample` rows of the workload; returns (seconds, bytes)."""
+    import oracle
+    xs = x_full[:rows_sample].float().numpy()
+    cols = xs.shape[1]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        c, s = oracle.quantize(xs, oracle.E4M3)
+        oracle.dequantize(c, s, cols, oracle.E4M3)
+    dt = time.perf_counter() - t0
+    qb, db = headline_bytes(rows_sample, cols)
+    return dt, (qb + db) * reps
+
+
+def cpu_baseline(x_full: torch.Tensor, target_s: float = 10.0):
+    import oracle
+    threads = oracle.num_threads()
+    dt, _ = oracle_step_rate(8, x_full)
+    per_row = max(dt / 8, 1e-6)
+    rows = int(min(x_full.shape[0], max(8, target_s / per_row)))
+    dt, nbytes = oracle_step_rate(rows, x_full)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of 4096 rows of the bf16 4096x4096 workload (quantize + dequantize), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------- main
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: same metric and workload, each step a
+    bounded sample of rows, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    w = workloads.make(2)
+    x = w["x"]
+    dt, _ = oracle_step_rate(8, x)
+    per_row = max(dt / 8, 1e-6)
+    budget = 120.0
+    rows = int(max(1, min(4096, budget / max(1, args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        oracle_step_rate(rows, x)
+    total_t, total_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_step_rate(rows, x)
+        total_t += dt
+        total_b += nb
+    value = total_b / total_t / 1e9
+    sample = f"{rows} of 4096 rows of the bf16 4096x4096 workload per step (quantize + dequantize)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": HEADLINE, "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--gemm-steps", type=int, default=20)
+    ap.add_argument("--no-gemm", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    import bit_gemm_gb300 as mx
+    peaks = measured_peaks()
+    dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+
+    hl = bench_headline(mx, args.steps, args.warmup, world, peaks, dev_index)
+    e2e = bench_e2e(mx, hl, args.steps, world)
+    gemms = []
+    if not args.no_gemm:
+        for cfg in (3, 4, 5):
+            gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks))
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(hl["x_host"])
+
+    dom = hl[hl["dominant"]]
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get(f"{hl['dominant']}_mxfp8_4096")
+    line = {
+        "metric": METRIC, "value": hl["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": hl["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": HEADLINE, "rows": hl["rows"], "cols": hl["cols"],
+                   "bytes_per_step": hl["bytes"], "parallelism": f"replicas x{world}",
+                   "l2": f"rotating {hl['nsets']} buffer sets (> 3x L2) between steps",
+                   "timing": "CUDA graphs of the K steps, events on the launch stream"},
+        "hbm_frac": hl["value"] / world / peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "kernel": hl["dominant"], "achieved": dom["gbs"], "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": dom["frac"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"],
+                     "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"},
+        "kernels": {"quantize": hl["quantize"], "dequantize": hl["dequantize"]},
+        "block_matmul": gemms,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": hl["launches"],
+        "clocks": hl["clocks"],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,629 @@
+// mx_gemm.cu -- block_matmul on the sm_103a tensor cores (tcgen05, TMEM, TMA).
+//
+// block_matmul of "A Dialect Is a Set of Co-Designed Decisions: Designing for
+// MX Quantization in MLIR" ("The four ops", "The block axis", "The
+// accumulator operand"):  C <- C + A * B with A [M,K] and B given as Bt [N,K],
+// both blocked along the reduction axis K, so each block's two E8M0 scales
+// factor out of its partial sum -- exactly what the block-scaled MMA does in
+// hardware (kind::mxf8f6f4: K = 32 per instruction, one scale per row;
+// kind::mxf4: K = 64 per instruction, two scales per row).
+//
+// Kernel shape (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: A/B code tiles (128-byte swizzled, K-major) and
+//               the 512-byte scale tiles into a STAGES-deep shared-memory ring.
+//   warp 1      allocates TMEM; one lane copies the scale tiles to TMEM
+//               (tcgen05.cp) and issues the MMAs into an f32 TMEM accumulator.
+//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging ->
+//               TMA reduce-add into C (C += acc, performed at L2), so C is read
+//               and written in place with no extra pass.
+// Work is either whole 128 x BN tiles handed out round-robin (large shapes),
+// or equal slices of the (tile, k-stage) space per CTA (few-tile shapes such
+// as decode; partial sums meet in C through the same reduce-add).  For M <= 64
+// the operands are swapped (C^T = Bt * A^T) so the long N side fills the
+// 128-row MMA dimension.
+//
+// Every mbarrier wait is bounded (see mx_device.cuh); a CTA that gives up sets
+// the device error word, drains what it issued, frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "mx_device.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+__device__ unsigned int g_mx_device_error = 0;
+
+cudaError_t read_clear_device_error(unsigned* out, cudaStream_t st) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_mx_device_error, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return e;
+    if (*out) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_mx_device_error, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    return e;
+}
+
+namespace {
+
+constexpr int KIND_F8F6F4 = 0;  // kind::mxf8f6f4 (E4M3 x E4M3, mixed E4M3 / E2M1)
+constexpr int KIND_F4 = 1;      // kind::mxf4     (E2M1 x E2M1, packed)
+
+constexpr int kThreads = 192;
+constexpr int kBlockM = 128;
+constexpr int kRowBytes = 128;        // bytes of K per tile row per stage (one 128-B swizzle atom)
+constexpr int kMmaPerStage = 4;       // 4 MMAs of 32 bytes of K each
+constexpr int kAccCol = 0;            // accumulator columns [0, BN)
+constexpr int kSfCol = 256;           // scale-factor columns start here
+constexpr uint32_t kTmemCols = 512;
+
+struct GemmParams {
+    int32_t P, Q, K;       // rows of the MMA A operand, rows of the MMA B operand, reduction length
+    int32_t tiles_p, tiles_q;
+    int32_t k_stages;      // stages of 128 bytes of K
+    int32_t sf_groups;     // 4-block scale groups per 128-row scale tile (NB4 / 4)
+    int32_t mode;          // 0 = whole tiles round-robin, 1 = equal slices of (tile, stage)
+    int64_t total_units;   // tiles * k_stages
+    uint64_t wait_limit_ns;
+    uint32_t idesc;        // instruction descriptor without scale-factor ids
+    int32_t swap;          // 1: C(q, p) += acc(p, q)  (operands swapped)
+    int32_t use_tma_epi;   // 1: TMA reduce-add epilogue, 0: per-element atomics
+    float* C;
+    int64_t ldc;
+    const uint8_t* sfa;    // scales of the MMA A operand (tensor-core layout)
+    const uint8_t* sfb;    // scales of the MMA B operand
+    uint32_t tx_a, tx_b;   // bytes one stage's code load counts on its barrier
+};
+
+struct Work {
+    int32_t tp, tq, kb0, kb1;
+};
+
+// The iter-th unit of work of this CTA; identical in every role.
+__device__ __forceinline__ bool get_work(const GemmParams& p, int iter, Work& w) {
+    const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
+    int64_t tile;
+    if (p.mode == 0) {
+        tile = (int64_t)blockIdx.x + (int64_t)iter * gridDim.x;
+        if (tile >= tiles) return false;
+        w.kb0 = 0;
+        w.kb1 = p.k_stages;
+    } else {
+        const int64_t u0 = p.total_units * blockIdx.x / gridDim.x;
+        const int64_t u1 = p.total_units * (blockIdx.x + 1) / gridDim.x;
+        if (u0 >= u1) return false;
+        tile = u0 / p.k_stages + iter;
+        const int64_t b = tile * p.k_stages > u0 ? tile * p.k_stages : u0;
+        const int64_t e = (tile + 1) * p.k_stages < u1 ? (tile + 1) * p.k_stages : u1;
+        if (b >= e) return false;
+        w.kb0 = (int32_t)(b - tile * p.k_stages);
+        w.kb1 = (int32_t)(e - tile * p.k_stages);
+    }
+    w.tp = (int32_t)(tile % p.tiles_p);
+    w.tq = (int32_t)(tile / p.tiles_p);
+    return true;
+}
+
+template <int KIND, int BN, int STAGES, int SWAP>
+struct Cfg {
+    static constexpr int G = KIND == KIND_F4 ? 2 : 1;                 // scale groups per stage
+    static constexpr int SFB_TILES = BN > 128 ? 2 : 1;                // 128-row scale tiles in the B tile
+    static constexpr int A_BYTES = kBlockM * kRowBytes;               // 16 KB
+    static constexpr int B_BYTES = BN * kRowBytes;
+    static constexpr int SFA_BYTES = G * 512;
+    static constexpr int SFB_BYTES = G * SFB_TILES * 512;
+    static constexpr int SF_COLS_A = 4 * G;
+    static constexpr int SF_COLS_B = 4 * G * SFB_TILES;
+    static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
+    // epilogue staging per warp: 2 buffers
+    static constexpr int EPI_BUF = SWAP ? BN * 32 * 4 : 32 * 16 * 4;  // bytes per buffer
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
+    static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16;
+    static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;           // + alignment slack
+    static_assert(kSfCol + STAGES * SF_COLS_STAGE <= (int)kTmemCols, "TMEM columns");
+    static_assert(BN <= kSfCol, "accumulator columns");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
+template <int KIND, int BN, int STAGES, int SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
+    using C_ = Cfg<KIND, BN, STAGES, SWAP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C_::OFF_BAR);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tmem_full = empty + STAGES;
+    uint64_t* tmem_empty = tmem_full + 1;
+    uint64_t* mma_done = tmem_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned* err = &g_mx_device_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 4);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
+        if (p.use_tma_epi) prefetch_tensormap(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
+            uint32_t issued_phase = 0;
+            bool ok = true;
+            Work w;
+            for (int it = 0; ok && get_work(p, it, w); ++it) {
+                const int32_t p0 = w.tp * kBlockM;
+                const int32_t q0 = w.tq * BN;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    // scale groups present for this stage (the last stage of a
+                    // ragged K may need only the first)
+                    const int g_first = kb * C_::G;
+                    const int g_count = min(C_::G, p.sf_groups - g_first);
+                    const int sfb_tiles = min(C_::SFB_TILES, (p.Q + 127) / 128 - (q0 >> 7));
+                    const uint32_t bytes = p.tx_a + p.tx_b + g_count * 512 + sfb_tiles * g_count * 512;
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    tma_load_2d(smem + C_::OFF_A + stage * C_::A_BYTES, &tm_a, kb * kRowBytes, p0, &full[stage]);
+                    tma_load_2d(smem + C_::OFF_B + stage * C_::B_BYTES, &tm_b, kb * kRowBytes, q0, &full[stage]);
+                    const uint8_t* sa = p.sfa + ((int64_t)w.tp * p.sf_groups + g_first) * 512;
+                    bulk_load(smem + C_::OFF_SFA + stage * C_::SFA_BYTES, sa, g_count * 512, &full[stage]);
+                    for (int t = 0; t < sfb_tiles; ++t) {
+                        const uint8_t* sb = p.sfb + ((int64_t)((q0 >> 7) + t) * p.sf_groups + g_first) * 512;
+                        bulk_load(smem + C_::OFF_SFB + stage * C_::SFB_BYTES + t * C_::G * 512, sb,
+                                  g_count * 512, &full[stage]);
+                    }
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: wait (bounded) for our own loads still in flight
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, p.wait_limit_ns, err);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            Work w;
+            for (int it = 0; ok && get_work(p, it, w); ++it) {
+                if (*abort_flag || !mbar_wait(tmem_empty, acc_phase ^ 1, p.wait_limit_ns, err)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (*abort_flag || !mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int g_first = kb * C_::G;
+                    const int g_count = min(C_::G, p.sf_groups - g_first);
+                    const uint32_t sf_col = tmem + kSfCol + stage * C_::SF_COLS_STAGE;
+                    // scale tiles -> TMEM: SFA group g at sf_col + 4g;
+                    // SFB group g, row-tile t at sf_col + SF_COLS_A + 4(g*SFB_TILES + t)
+                    for (int g = 0; g < g_count; ++g) {
+                        const uint32_t sa = smem_u32(smem + C_::OFF_SFA + stage * C_::SFA_BYTES + g * 512);
+                        tc_cp_32x128b_warpx4(sf_col + 4 * g, smem_desc(sa, 0, 128, 0));
+                        for (int t = 0; t < C_::SFB_TILES; ++t) {
+                            const uint32_t sb =
+                                smem_u32(smem + C_::OFF_SFB + stage * C_::SFB_BYTES + t * C_::G * 512 + g * 512);
+                            tc_cp_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (g * C_::SFB_TILES + t),
+                                                 smem_desc(sb, 0, 128, 0));
+                        }
+                    }
+                    const uint32_t a_base = smem_u32(smem + C_::OFF_A + stage * C_::A_BYTES);
+                    const uint32_t b_base = smem_u32(smem + C_::OFF_B + stage * C_::B_BYTES);
+                    // valid MMAs in this stage (ragged K): each consumes 32 bytes of K
+                    const int64_t k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
+                    const int64_t k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
+                    const int64_t rem = (int64_t)p.K - (int64_t)kb * k_elem_per_stage;
+                    const int64_t need = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
+                    const int n_mma = need < kMmaPerStage ? (int)need : kMmaPerStage;
+                    for (int i = 0; i < n_mma; ++i) {
+                        const uint64_t adesc = smem_desc(a_base + i * 32, 0, 1024, 2);
+                        const uint64_t bdesc = smem_desc(b_base + i * 32, 0, 1024, 2);
+                        int g, sf_id;
+                        if (KIND == KIND_F4) {
+                            g = i >> 1;           // MMA i covers blocks 2i, 2i+1 of the stage
+                            sf_id = (i & 1) * 2;
+                        } else {
+                            g = 0;                // MMA i covers block i of the stage
+                            sf_id = i;
+                        }
+                        const uint32_t idesc = p.idesc | ((uint32_t)sf_id << 4) | ((uint32_t)sf_id << 29);
+                        const uint32_t sfa = sf_col + 4 * g;
+                        const uint32_t sfb = sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES;
+                        const uint32_t acc = (kb > w.kb0 || i > 0) ? 1u : 0u;
+                        if (KIND == KIND_F4)
+                            mma_mxf4(tmem + kAccCol, adesc, bdesc, idesc, sfa, sfb, acc);
+                        else
+                            mma_mxf8f6f4(tmem + kAccCol, adesc, bdesc, idesc, sfa, sfb, acc);
+                    }
+                    tc_commit(&empty[stage]);  // stage free once these MMAs have read it
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tmem_full);
+                acc_phase ^= 1;
+            }
+            // every tcgen05 op issued by this thread completes before TMEM is freed
+            tc_commit(mma_done);
+            mbar_wait(mma_done, 0, p.wait_limit_ns, err);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may read
+        uint8_t* stage_buf = smem + C_::OFF_EPI + (warp - 2) * 2 * C_::EPI_BUF;
+        uint32_t acc_phase = 0;
+        int nbuf = 0;  // chunks issued so far by this warp (buffer = nbuf & 1)
+        Work w;
+        for (int it = 0; get_work(p, it, w); ++it) {
+            bool ok = !*abort_flag && mbar_wait(tmem_full, acc_phase, p.wait_limit_ns, err);
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int32_t p0 = w.tp * kBlockM + 32 * q;  // first MMA-A row of this warp
+            const int32_t q0 = w.tq * BN;
+            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + kAccCol;
+            if (SWAP) {
+                // lane i holds acc(p0 + i, q0 + j), j < BN  ->  C[q0 + j][p0 + i]
+                uint32_t r[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 16; ++c) {
+                    uint32_t t[16];
+                    tmem_ld_32x32b_x16(t_row + 16 * c, t);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[16 * c + j] = t[j];
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tmem_empty);
+                if (p.use_tma_epi) {
+                    uint8_t* buf = stage_buf + (nbuf & 1) * C_::EPI_BUF;
+                    if (nbuf >= 2 && lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    float* f = reinterpret_cast<float*>(buf);
+#pragma unroll
+                    for (int j = 0; j < BN; ++j) f[j * 32 + lane] = __uint_as_float(r[j]);  // [BN rows][32 cols]
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_2d(&tm_c, buf, p0, q0);
+                        bulk_commit_group();
+                    }
+                    ++nbuf;
+                } else {
+                    const int32_t pr = p0 + lane;
+                    if (pr < p.P) {
+#pragma unroll
+                        for (int j = 0; j < BN; ++j)
+                            if (q0 + j < p.Q) atomicAdd(p.C + (int64_t)(q0 + j) * p.ldc + pr, __uint_as_float(r[j]));
+                    }
+                }
+            } else {
+                const int nchunks = BN / 16;
+                const int32_t pr = p0 + lane;
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + 16 * c, r);
+                    tmem_ld_wait();
+                    if (c == nchunks - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tmem_empty);
+                    }
+                    if (q0 + 16 * c >= p.Q) continue;  // chunk wholly past N
+                    if (p.use_tma_epi) {
+                        uint8_t* buf = stage_buf + (nbuf & 1) * C_::EPI_BUF;
+                        if (nbuf >= 2 && lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                        // [32 rows][16 f32] with the 64-byte swizzle: 16-B chunk j of
+                        // row i sits at chunk j ^ ((i >> 1) & 3)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int js = j ^ ((lane >> 1) & 3);
+                            uint4 v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                            *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = v;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_2d(&tm_c, buf, q0 + 16 * c, p0);
+                            bulk_commit_group();
+                        }
+                        ++nbuf;
+                    } else if (pr < p.P) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (q0 + 16 * c + j < p.Q)
+                                atomicAdd(p.C + (int64_t)pr * p.ldc + q0 + 16 * c + j, __uint_as_float(r[j]));
+                    }
+                }
+            }
+            acc_phase ^= 1;
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map over the codes of an operand with `rows` rows of K elements.
+// fmt_kind: 0 = one byte per element (E4M3), 1 = packed E2M1 as bytes,
+// 2 = packed E2M1 expanded to one byte per element in shared memory.
+bool make_operand_map(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int fmt_kind, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2];
+    cuuint64_t strides[1];
+    cuuint32_t box[2] = {(cuuint32_t)kRowBytes, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (fmt_kind == 0) {
+        dims[0] = (cuuint64_t)K;
+        strides[0] = (cuuint64_t)K;
+    } else if (fmt_kind == 1) {
+        dims[0] = (cuuint64_t)(K / 2);
+        strides[0] = (cuuint64_t)(K / 2);
+    } else {
+        dt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+        dims[0] = (cuuint64_t)K;  // counted in 4-bit elements
+        strides[0] = (cuuint64_t)(K / 2);
+    }
+    dims[1] = (cuuint64_t)rows;
+    CUresult r = enc(m, dt, 2, const_cast<void*>(codes), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Tensor map over C (rows x cols f32, row-major) for the reduce-add epilogue.
+bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_cols, int box_rows, bool swz64) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * 4)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Instruction descriptor (block-scaled kinds), scale-factor ids left 0:
+//   [7,10) A type  [10,13) B type  [15] A K-major(0)  [16] B K-major(0)
+//   [17,23) N>>3   [23] scale type UE8M0 (1)   [24,29) M>>4
+uint32_t make_idesc(int kind, int a_fmt, int b_fmt, int n) {
+    auto code = [&](int f) -> uint32_t {
+        if (kind == KIND_F4) return 1u;          // E2M1 in kind::mxf4
+        return f == FMT_E2M1 ? 5u : 0u;          // kind::mxf8f6f4: E2M1 = 5, E4M3 = 0
+    };
+    uint32_t d = 0;
+    d |= code(a_fmt) << 7;
+    d |= code(b_fmt) << 10;
+    d |= (uint32_t)(n >> 3) << 17;
+    d |= 1u << 23;
+    d |= (uint32_t)(kBlockM >> 4) << 24;
+    return d;
+}
+
+template <int KIND, int BN, int STAGES, int SWAP>
+cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p, int grid,
+                cudaStream_t st) {
+    using C_ = Cfg<KIND, BN, STAGES, SWAP>;
+    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP>;
+    static int configured_for = -1;  // per-instantiation attribute (process-wide; one value for all devices)
+    if (configured_for != C_::SMEM) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM);
+        if (e != cudaSuccess) return e;
+        configured_for = C_::SMEM;
+    }
+    kern<<<grid, kThreads, C_::SMEM, st>>>(ta, tb, tc, p);
+    return cudaGetLastError();
+}
+
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+        // nothing ever arrives on `bar`: this wait must give up and report
+        mbar_wait(&bar, 0, limit_ns, &g_mx_device_error);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char** detail) {
+    *detail = nullptr;
+    const bool swap = a.M <= 64 && a.N > a.M;
+    // MMA orientation: operand X = rows along the 128-row MMA dimension.
+    const void* x_codes = swap ? a.b_codes : a.a_codes;
+    const uint8_t* x_sf = swap ? a.b_scales : a.a_scales;
+    const int x_fmt = swap ? a.b_fmt : a.a_fmt;
+    const int64_t P = swap ? a.N : a.M;
+    const void* y_codes = swap ? a.a_codes : a.b_codes;
+    const uint8_t* y_sf = swap ? a.a_scales : a.b_scales;
+    const int y_fmt = swap ? a.a_fmt : a.b_fmt;
+    const int64_t Q = swap ? a.M : a.N;
+
+    if (a.scale_layout != LAYOUT_MMA) {
+        *detail = "row-major scales are not accepted by block_matmul yet; use MX_SCALES_MMA or mx_scales_relayout";
+        return cudaErrorNotSupported;
+    }
+    const int kind = (x_fmt == FMT_E2M1 && y_fmt == FMT_E2M1) ? KIND_F4 : KIND_F8F6F4;
+    const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
+
+    int bn;
+    if (swap) {
+        bn = (int)round_up(Q, 16);  // 16..64
+    } else {
+        bn = Q <= 128 ? 128 : 256;
+    }
+
+    auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
+    CUtensorMap ta, tb, tc;
+    if (!make_operand_map(&ta, x_codes, P, a.K, fk(x_fmt), kBlockM) ||
+        !make_operand_map(&tb, y_codes, Q, a.K, fk(y_fmt), bn)) {
+        *detail = "cuTensorMapEncodeTiled rejected an operand";
+        return cudaErrorInvalidValue;
+    }
+    const bool tma_epi = (a.N % 4) == 0;
+    std::memset(&tc, 0, sizeof(tc));
+    if (tma_epi) {
+        bool okc = swap ? make_c_map(&tc, a.C, a.M, a.N, 32, bn, false) : make_c_map(&tc, a.C, a.M, a.N, 16, 32, true);
+        if (!okc) {
+            *detail = "cuTensorMapEncodeTiled rejected C";
+            return cudaErrorInvalidValue;
+        }
+    }
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.P = (int32_t)P;
+    p.Q = (int32_t)Q;
+    p.K = (int32_t)a.K;
+    p.tiles_p = (int32_t)((P + kBlockM - 1) / kBlockM);
+    p.tiles_q = (int32_t)((Q + bn - 1) / bn);
+    p.k_stages = (int32_t)((a.K + k_per_stage - 1) / k_per_stage);
+    p.sf_groups = (int32_t)(round_up(a.K / 32, 4) / 4);
+    p.wait_limit_ns = wait_limit_ns();
+    p.idesc = make_idesc(kind, x_fmt, y_fmt, bn);
+    p.swap = swap ? 1 : 0;
+    p.use_tma_epi = tma_epi ? 1 : 0;
+    p.C = a.C;
+    p.ldc = a.N;
+    p.sfa = x_sf;
+    p.sfb = y_sf;
+    // A load of 4-bit codes expanded to one byte each in shared memory
+    // (16U4_ALIGN16B) completes with the packed byte count: 64 B per row.
+    p.tx_a = (uint32_t)kBlockM * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.tx_b = (uint32_t)bn * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
+    p.total_units = tiles * p.k_stages;
+    const int sms = sm_count();
+    int grid;
+    if (tiles >= sms || p.k_stages < 4) {
+        p.mode = 0;
+        grid = (int)(tiles < sms ? tiles : sms);
+    } else {
+        p.mode = 1;  // slices of (tile, stage): keeps every SM streaming
+        grid = (int)(p.total_units < sms ? p.total_units : sms);
+    }
+
+#define MX_RUN(KIND_, BN_, ST_, SW_) return run<KIND_, BN_, ST_, SW_>(ta, tb, tc, p, grid, st)
+    if (swap) {
+        if (kind == KIND_F4) {
+            if (bn == 16) MX_RUN(KIND_F4, 16, 8, 1);
+            if (bn == 32) MX_RUN(KIND_F4, 32, 8, 1);
+            if (bn == 48) MX_RUN(KIND_F4, 48, 6, 1);
+            MX_RUN(KIND_F4, 64, 6, 1);
+        } else {
+            if (bn == 16) MX_RUN(KIND_F8F6F4, 16, 8, 1);
+            if (bn == 32) MX_RUN(KIND_F8F6F4, 32, 8, 1);
+            if (bn == 48) MX_RUN(KIND_F8F6F4, 48, 6, 1);
+            MX_RUN(KIND_F8F6F4, 64, 6, 1);
+        }
+    }
+    if (kind == KIND_F4) {
+        if (bn == 128) MX_RUN(KIND_F4, 128, 6, 0);
+        MX_RUN(KIND_F4, 256, 4, 0);
+    }
+    if (bn == 128) MX_RUN(KIND_F8F6F4, 128, 6, 0);
+    MX_RUN(KIND_F8F6F4, 256, 4, 0);
+#undef MX_RUN
+}
+
+}  // namespace mx

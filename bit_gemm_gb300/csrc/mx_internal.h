@@ -1,0 +1,50 @@
+// mx_internal.h -- launchers shared between the C-ABI layer and the kernels.
+// Arguments are already validated by the caller (mx_abi.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+enum Fmt : int { FMT_E2M1 = 1, FMT_E4M3 = 2 };
+enum Layout : int { LAYOUT_ROWMAJOR = 0, LAYOUT_MMA = 1 };
+enum DType : int { DT_F32 = 1, DT_BF16 = 2 };
+
+// Offset of scale (r, j) in the tensor-core scale layout; nb4 = blocks per
+// row rounded up to a multiple of 4.
+__host__ __device__ inline int64_t mma_scale_offset(int64_t r, int64_t j, int64_t nb4) {
+    return ((r >> 7) * (nb4 >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+__host__ __device__ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+cudaError_t launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, void* codes,
+                            uint8_t* scales, int layout, cudaStream_t stream);
+cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols, int fmt,
+                              int layout, float* y, cudaStream_t stream);
+cudaError_t launch_relayout(const uint8_t* src, int src_layout, int64_t rows, int64_t cols, uint8_t* dst,
+                            int dst_layout, cudaStream_t stream);
+
+struct GemmArgs {
+    const void* a_codes;
+    const uint8_t* a_scales;
+    int a_fmt;
+    const void* b_codes;
+    const uint8_t* b_scales;
+    int b_fmt;
+    int scale_layout;
+    int64_t M, N, K;
+    float* C;
+};
+// Returns cudaSuccess or an error; *detail gets a static explanation on failure.
+cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t stream, const char** detail);
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+// Limit (ns) for every bounded wait inside the library's kernels.
+uint64_t wait_limit_ns();
+
+int sm_count();
+
+}  // namespace mx

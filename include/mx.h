@@ -1,0 +1,185 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) MX block-scaled quantization library.
+ *
+ * The library implements the hot path of OCP Microscaling (MX) block scaling:
+ * quantize a float tensor into low-bit element codes plus one power-of-two
+ * E8M0 scale per block of 32 consecutive elements along the last (reduction)
+ * axis, dequantize it back exactly, and multiply two block-scaled operands
+ * into an f32 accumulator that is both an input and the output.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [Dialect] "A Dialect Is a Set of Co-Designed Decisions: Designing for MX
+ *             Quantization in MLIR" -- "The type: !mx.tensor", "The four ops",
+ *             "The block axis", "The accumulator operand".
+ *   [Layout]  "Bit Layout" (MXFP4 community format pages) -- "The E2M1
+ *             element", "The E8M0 shared scale", "Block structure and
+ *             packing", "Reference encode and decode".
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers, owned by the caller.  The
+ *     library allocates no device memory and keeps no pointer after a call
+ *     returns.  Outputs are written in place (destination passing, [Dialect]
+ *     "The accumulator operand").
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on that stream.  Argument checks happen
+ *     on the host before anything is launched; a failed check returns an error
+ *     and launches nothing.
+ *   - Tensors are row-major and dense.  A tensor of `rows` x `cols` is blocked
+ *     along `cols`; `cols` must be a multiple of the block size 32 (the type
+ *     verifier's rule: the block size divides the last dimension, [Dialect]
+ *     "The type: !mx.tensor").  Zero rows or zero cols is a valid no-op.
+ *   - block_size must be 32 and scale_type MX_SCALE_E8M0; anything else is
+ *     MX_ERR_UNSUPPORTED.
+ *   - Pointers must be 16-byte aligned (MX_ERR_ALIGN) unless stated.
+ *   - There is no CPU fallback: without a usable CUDA device every compute
+ *     call returns MX_ERR_CUDA or MX_ERR_NO_DEVICE.
+ *
+ * Element codes ([Layout] "The E2M1 element", "Block structure and packing")
+ *   MX_E2M1   (MXFP4): 4-bit code S.EE.M, bias 1, magnitudes
+ *             {0, .5, 1, 1.5, 2, 3, 4, 6}; two codes per byte, element 2k in
+ *             the LOW nibble and element 2k+1 in the high nibble.  A row of
+ *             `cols` elements is cols/2 bytes.
+ *   MX_E4M3FN (MXFP8): 8-bit code S.EEEE.MMM, bias 7, largest finite 448,
+ *             S.1111.111 is NaN, no infinities.  One byte per element.
+ *
+ * Scales ([Layout] "The E8M0 shared scale")
+ *   One E8M0 byte b per block: value 2^(b-127); b = 0xFF is NaN and turns
+ *   every element of its block into NaN.  Two layouts:
+ *   MX_SCALES_ROWMAJOR: [rows][cols/32] bytes, row-major (the public layout).
+ *   MX_SCALES_MMA: the tensor-core operand layout.  Rows are padded to a
+ *     multiple of 128 and blocks per row to a multiple of 4; scale (r, j)
+ *     (row r, block j) is the byte at
+ *       ((r/128) * (NB4/4) + j/4) * 512 + (r%32)*16 + ((r/32)%4)*4 + (j%4)
+ *     where NB4 = blocks per row rounded up to a multiple of 4.  Padding bytes
+ *     are written as 0 by mx_quantize.  Size: mx_scales_bytes().
+ *
+ * Rounding ([Layout] "Reference encode and decode"; readings where the pages
+ * are silent are marked *)
+ *   amax = max |x| over the block; an all-zero block gets codes 0 and scale
+ *   127.  e = floor(log2 amax) - emax (emax 2 for E2M1, 8* for E4M3FN), with
+ *   floor(log2) the exact integer exponent*, clipped to [-127, 127]; scale
+ *   byte e + 127.  Each element goes to the nearest grid magnitude of
+ *   |x| / 2^e, ties to the LOWER magnitude*, saturating at the largest finite
+ *   magnitude; the sign bit is set when x < 0.  A block holding a NaN or an
+ *   infinity gets scale 0xFF and codes 0*.
+ */
+#ifndef MX_H
+#define MX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MX_API __attribute__((visibility("default")))
+#else
+#define MX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MX_OK = 0,
+    MX_ERR_NULL = 1,        /* a required pointer is NULL */
+    MX_ERR_SHAPE = 2,       /* negative dimension, cols % 32 != 0, or a shape rule below */
+    MX_ERR_UNSUPPORTED = 3, /* block_size != 32, scale type, format/dtype/layout value, aliasing */
+    MX_ERR_ALIGN = 4,       /* pointer misaligned for the call */
+    MX_ERR_TIMEOUT = 5,     /* a kernel gave up waiting (reported by mx_device_status) */
+    MX_ERR_CUDA = 6,        /* a CUDA runtime or driver call failed */
+    MX_ERR_NO_DEVICE = 7    /* no sm_103 device is current */
+} mx_status_t;
+
+typedef enum { MX_E2M1 = 1, MX_E4M3FN = 2 } mx_format_t;
+typedef enum { MX_SCALE_E8M0 = 1 } mx_scale_type_t;
+typedef enum { MX_F32 = 1, MX_BF16 = 2 } mx_dtype_t;
+typedef enum { MX_SCALES_ROWMAJOR = 0, MX_SCALES_MMA = 1 } mx_scale_layout_t;
+
+/* Bytes of element codes for a rows x cols tensor in format fmt
+ * (rows*cols/2 for E2M1, rows*cols for E4M3FN); -1 on a bad argument. */
+MX_API int64_t mx_codes_bytes(mx_format_t fmt, int64_t rows, int64_t cols);
+
+/* Bytes of scales for a rows x cols tensor in the given scale layout
+ * (rows*cols/32 row-major; the padded size for MX_SCALES_MMA); -1 on a bad
+ * argument.  One scale per block: the count is a property of the type, not
+ * of the data ([Dialect] "The type: !mx.tensor", getNumScaleBlocks). */
+MX_API int64_t mx_scales_bytes(mx_scale_layout_t layout, int64_t rows, int64_t cols);
+
+/* quantize_block over a whole tensor ([Dialect] "The four ops";
+ * [Layout] "Reference encode and decode").
+ *   x       : rows x cols input, f32 or bf16 (x_dtype), row-major, 16-B aligned.
+ *   codes   : out, mx_codes_bytes(fmt, rows, cols) bytes, 16-B aligned.
+ *   scales  : out, mx_scales_bytes(scale_layout, rows, cols) bytes; 4-B
+ *             aligned for MX_SCALES_ROWMAJOR, 16-B for MX_SCALES_MMA.
+ * Codes and scales are bit-exact functions of x (see "Rounding" above). */
+MX_API mx_status_t mx_quantize(const void* x, mx_dtype_t x_dtype, int64_t rows, int64_t cols,
+                        mx_format_t fmt, int block_size, mx_scale_type_t scale_type,
+                        void* codes, uint8_t* scales, mx_scale_layout_t scale_layout,
+                        void* stream);
+
+/* dequantize_block over a whole tensor ([Dialect] "The four ops": back to
+ * f32; [Layout] "The E8M0 shared scale").  y[r][c] = element * 2^(b-127),
+ * exact (no rounding step); b = 0xFF gives NaN for the whole block, as does
+ * an E4M3FN NaN code for its element.  Subnormal results are kept.
+ *   codes, scales : as written by mx_quantize (same fmt and scale_layout).
+ *   y             : out, rows x cols f32, row-major, 16-B aligned. */
+MX_API mx_status_t mx_dequantize(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                          mx_format_t fmt, int block_size, mx_scale_type_t scale_type,
+                          mx_scale_layout_t scale_layout, float* y, void* stream);
+
+/* block_matmul ([Dialect] "The four ops", "The block axis", "The accumulator
+ * operand"): C <- C + A * B, multiplied while both operands are still block
+ * scaled, accumulated in f32 on the tensor cores, C updated in place.
+ *   A : M x K, codes a_codes (format a_fmt) and scales a_scales, blocked
+ *       along K.
+ *   B : K x N, passed TRANSPOSED as an N x K tensor (b_codes, b_scales,
+ *       format b_fmt) so that it too is blocked along its reduction axis K
+ *       ([Dialect] "The block axis": the law is reduction-axis blocking).
+ *   scale_layout : layout of both a_scales and b_scales.  MX_SCALES_MMA is the
+ *       fast path; MX_SCALES_ROWMAJOR is accepted as well.
+ *   C : M x N f32, row-major, read and written in place; must not overlap an
+ *       input (MX_ERR_UNSUPPORTED).
+ * Formats: any pair of MX_E2M1 / MX_E4M3FN.  Shape rules: K % 32 == 0; when
+ * exactly one operand is MX_E2M1, K % 128 == 0 and that operand's codes must
+ * be 32-B aligned.
+ * Result: C[m][n] + sum_k deqA[m][k] * deqB[n][k], summed in f32 (order
+ * unspecified; the parity bound is 1e-5 * sum_k |deqA*deqB|).  A NaN scale
+ * or NaN code reaches the outputs that use it.  f32 subnormal results may be
+ * flushed to zero by the tensor-core and reduction hardware. */
+MX_API mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt,
+                            const void* b_codes, const uint8_t* b_scales, mx_format_t b_fmt,
+                            mx_scale_layout_t scale_layout, int block_size,
+                            mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
+                            float* C, void* stream);
+
+/* Re-lay scales between MX_SCALES_ROWMAJOR and MX_SCALES_MMA (both
+ * directions; identical layouts copy).  src and dst must not overlap; sizes
+ * as mx_scales_bytes().  The scale values are not changed. */
+MX_API mx_status_t mx_scales_relayout(const uint8_t* src, mx_scale_layout_t src_layout, int64_t rows,
+                               int64_t cols, uint8_t* dst, mx_scale_layout_t dst_layout,
+                               void* stream);
+
+/* Synchronize `stream`, then report and clear the device-side error word
+ * that kernels set when a bounded wait gives up (MX_ERR_TIMEOUT), or the
+ * stream's CUDA error (MX_ERR_CUDA).  MX_OK when neither happened. */
+MX_API mx_status_t mx_device_status(void* stream);
+
+/* Failure-detection self test: launches one block that waits on a barrier
+ * nothing will ever complete, giving up after `limit_ns` nanoseconds
+ * (1e3..1e10); the kernel then sets the error word and returns normally, so
+ * the context stays usable.  mx_device_status() afterwards must report
+ * MX_ERR_TIMEOUT. */
+MX_API mx_status_t mx_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Static text for a status code. */
+MX_API const char* mx_status_string(mx_status_t status);
+
+/* Text describing the last error returned on the calling host thread
+ * (empty string if none). */
+MX_API const char* mx_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_H */

