@@ -303,10 +303,10 @@ def bench_e2e(mx, hl, steps, world):
             "h2d_bytes_per_step": rows * cols * 2, "d2h_bytes_per_step": rows * cols * 4, "steps": n}
 
 
-def bench_gemm(mx, cfg, steps, warmup, world, peaks):
+def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0):
     """block_matmul workloads.  Weights are quantized before timing; the step
     includes the activation quantize where the workload quantizes on the fly."""
-    w = workloads.make(cfg)
+    w = workloads.make(cfg, scale=scale)
     M, N, K = w["M"], w["N"], w["K"]
     if cfg == 3:
         fa, fb, a_key, b_key, quant_a, kind = mx.E4M3FN, mx.E2M1, "A", "W", True, "fp8"
@@ -447,6 +447,10 @@ def main():
     ap.add_argument("--gemm-steps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", choices=["headline", "decode", "square", "prefill"], default=None,
+                    help="run one workload only, print its numbers and exit (profiling runs)")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="row-count scale of the GEMM workloads with --only (1 = full size)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -462,6 +466,16 @@ def main():
     dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
 
+    if args.only is not None:
+        if args.only == "headline":
+            hl = bench_headline(mx, args.steps, args.warmup, world, peaks, dev_index)
+            out = {k: v for k, v in hl.items() if k not in ("x_host",)}
+        else:
+            cfg = {"decode": 3, "square": 4, "prefill": 5}[args.only]
+            out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale)
+        if rank == 0:
+            print(json.dumps(out, default=str), flush=True)
+        return
     hl = bench_headline(mx, args.steps, args.warmup, world, peaks, dev_index)
     e2e = bench_e2e(mx, hl, args.steps, world)
     gemms = []
