@@ -136,6 +136,12 @@ __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Fire-and-forget vector add of four f32 into global memory (at L2).
+__device__ __forceinline__ void red_add_v4(float* ptr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // TMEM allocation: the whole warp executes these.

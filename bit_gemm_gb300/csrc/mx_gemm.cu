@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -56,12 +57,10 @@ namespace {
 constexpr int KIND_F8F6F4 = 0;  // kind::mxf8f6f4 (E4M3 x E4M3, mixed E4M3 / E2M1)
 constexpr int KIND_F4 = 1;      // kind::mxf4     (E2M1 x E2M1, packed)
 
-constexpr int kThreads = 192;
 constexpr int kBlockM = 128;
 constexpr int kRowBytes = 128;        // bytes of K per tile row per stage (one 128-B swizzle atom)
 constexpr int kMmaPerStage = 4;       // 4 MMAs of 32 bytes of K each
-constexpr int kAccCol = 0;            // accumulator columns [0, BN)
-constexpr int kSfCol = 256;           // scale-factor columns start here
+constexpr int kAccCol = 0;            // accumulator buffers at columns [0, ACC * BN)
 constexpr uint32_t kTmemCols = 512;
 
 struct GemmParams {
@@ -74,7 +73,9 @@ struct GemmParams {
     uint64_t wait_limit_ns;
     uint32_t idesc;        // instruction descriptor without scale-factor ids
     int32_t swap;          // 1: C(q, p) += acc(p, q)  (operands swapped)
-    int32_t use_tma_epi;   // 1: TMA reduce-add epilogue, 0: per-element atomics
+    int32_t use_tma_epi;   // 1: C map valid (TMA reduce-add epilogue), 0: per-element atomics
+    int32_t epi_red_v4;    // 1: write C with vector reductions instead of TMA (BN = 256 path)
+    int32_t k_rotate;      // 1: rotate each tile's K loop by its M-tile index
     float* C;
     int64_t ldc;
     const uint8_t* sfa;    // scales of the MMA A operand (tensor-core layout)
@@ -84,6 +85,7 @@ struct GemmParams {
 
 struct Work {
     int32_t tp, tq, kb0, kb1;
+    int32_t rot;  // the K loop starts `rot` stages into [kb0, kb1) and wraps
 };
 
 // The iter-th unit of work of this CTA; identical in every role.
@@ -108,13 +110,27 @@ __device__ __forceinline__ bool get_work(const GemmParams& p, int iter, Work& w)
     }
     w.tp = (int32_t)(tile % p.tiles_p);
     w.tq = (int32_t)(tile / p.tiles_p);
+    // Concurrently running tiles share a B tile and differ in their M tile;
+    // starting each M tile at a different K stage keeps them from requesting
+    // the same lines of B at the same moment.  Only the order of the f32
+    // partial sums changes.
+    w.rot = (p.mode == 0 && p.k_rotate) ? (int32_t)(((int64_t)w.tp * (w.kb1 - w.kb0)) / p.tiles_p) : 0;
     return true;
 }
 
-template <int KIND, int BN, int STAGES, int SWAP>
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0>
 struct Cfg {
     static constexpr int G = KIND == KIND_F4 ? 2 : 1;                 // scale groups per stage
-    static constexpr int SFB_TILES = BN > 128 ? 2 : 1;                // 128-row scale tiles in the B tile
+    // 128-row scale tiles covering the BN rows of a B tile (tiles start on
+    // 128-row boundaries: scale-factor TMEM addresses must stay aligned)
+    static constexpr int SFB_TILES = (BN + 127) / 128;
+    // TMEM accumulator buffers: two 128-column buffers for BN = 128; for BN = 256
+    // the single buffer is drained into the registers of eight epilogue warps
+    // (two per TMEM lane quarter, 128 columns each) and released at once, so
+    // the next tile's MMAs overlap the write-out of this one
+    static constexpr int ACC = (!SWAP && 2 * BN <= 256) ? 2 : 1;
+    static constexpr int EPI_WARPS = (!SWAP && BN == 256) ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int A_BYTES = kBlockM * kRowBytes;               // 16 KB
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int SFA_BYTES = G * 512;
@@ -122,34 +138,46 @@ struct Cfg {
     static constexpr int SF_COLS_A = 4 * G;
     static constexpr int SF_COLS_B = 4 * G * SFB_TILES;
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
-    // epilogue staging per warp: 2 buffers
-    static constexpr int EPI_BUF = SWAP ? BN * 32 * 4 : 32 * 16 * 4;  // bytes per buffer
+    static constexpr int SF_COL0 = ACC * BN > 256 ? ACC * BN : 256;   // first scale column
+    // scale slots in TMEM; a slot is rewritten by tcgen05.cp only after the
+    // MMAs that read it were issued (tcgen05 operations of one thread execute
+    // in issue order)
+    static constexpr int SF_SLOTS_FIT = ((int)kTmemCols - SF_COL0) / SF_COLS_STAGE;
+    static constexpr int SF_SLOTS = SF_SLOTS_FIT < STAGES ? SF_SLOTS_FIT : STAGES;
+    // epilogue staging per warp: NBUF buffers of 32 rows x 32 f32 (non-swapped)
+    // or BN rows x 32 f32 (swapped)
+    static constexpr int NBUF = NBUF_ ? NBUF_ : (EPI_WARPS == 8 ? 1 : 2);
+    static constexpr int EPI_COLS = SWAP ? 32 : (EPI_WARPS == 8 ? 16 : 32);   // C columns per staged box
+    static constexpr int EPI_BUF = SWAP ? BN * 32 * 4 : 32 * EPI_COLS * 4;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
-    static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * NBUF * EPI_BUF;
+    static constexpr int BAR_BYTES = (2 * STAGES + 2 * ACC + 1) * 8 + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;           // + alignment slack
-    static_assert(kSfCol + STAGES * SF_COLS_STAGE <= (int)kTmemCols, "TMEM columns");
-    static_assert(BN <= kSfCol, "accumulator columns");
+    static_assert(SF_SLOTS >= 2, "at least two scale slots in TMEM");
+    static_assert(SF_COL0 + SF_SLOTS * SF_COLS_STAGE <= (int)kTmemCols, "TMEM columns");
+    static_assert(ACC * BN <= SF_COL0, "accumulator columns");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
-template <int KIND, int BN, int STAGES, int SWAP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_>
+__global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    using C_ = Cfg<KIND, BN, STAGES, SWAP>;
+    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_>;
+    constexpr int ACC = C_::ACC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C_::OFF_BAR);
     uint64_t* empty = full + STAGES;
-    uint64_t* tmem_full = empty + STAGES;
-    uint64_t* tmem_empty = tmem_full + 1;
-    uint64_t* mma_done = tmem_empty + 1;
+    uint64_t* tmem_full = empty + STAGES;   // [ACC]
+    uint64_t* tmem_empty = tmem_full + ACC;  // [ACC]
+    uint64_t* mma_done = tmem_empty + ACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -162,8 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 4);
+        for (int a = 0; a < ACC; ++a) {
+            mbar_init(&tmem_full[a], 1);
+            mbar_init(&tmem_empty[a], C_::EPI_WARPS);
+        }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -192,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0; ok && get_work(p, it, w); ++it) {
                 const int32_t p0 = w.tp * kBlockM;
                 const int32_t q0 = w.tq * BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                const int nk = w.kb1 - w.kb0;
+                for (int j = 0; j < nk; ++j) {
+                    const int kb = w.kb0 + (j + w.rot) % nk;
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err)) {
                         *abort_flag = 1;
                         ok = false;
@@ -202,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // ragged K may need only the first)
                     const int g_first = kb * C_::G;
                     const int g_count = min(C_::G, p.sf_groups - g_first);
+                    // scale row-tiles covering rows [q0, q0 + BN), clipped to the tensor
                     const int sfb_tiles = min(C_::SFB_TILES, (p.Q + 127) / 128 - (q0 >> 7));
                     const uint32_t bytes = p.tx_a + p.tx_b + g_count * 512 + sfb_tiles * g_count * 512;
                     mbar_arrive_expect_tx(&full[stage], bytes);
@@ -231,67 +264,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
+            // Everything that does not depend on the stage is built once: the
+            // shared-memory descriptors of stage 0 (a stage's descriptors differ
+            // only in the start-address field, which is advanced by adds) and
+            // the four instruction descriptors carrying the scale-factor ids.
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
+            const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
+            const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFB), 0, 128, 0);
+            uint32_t idesc[kMmaPerStage];
+#pragma unroll
+            for (int i = 0; i < kMmaPerStage; ++i) {
+                // kind::mxf4: MMA i covers blocks 2i, 2i+1 of the stage (scale bytes
+                // 0-1 or 2-3 of its group); kind::mxf8f6f4: block i (byte i)
+                const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
+                idesc[i] = p.idesc | (sf_id << 4) | (sf_id << 29);
+            }
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t acc_phase = 0;
+            int sf_slot = 0;
             bool ok = true;
             Work w;
             for (int it = 0; ok && get_work(p, it, w); ++it) {
-                if (*abort_flag || !mbar_wait(tmem_empty, acc_phase ^ 1, p.wait_limit_ns, err)) {
+                const int acc = it % ACC;
+                const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
+                if (*abort_flag || !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.wait_limit_ns, err)) {
                     *abort_flag = 1;
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                const uint32_t d_tmem = tmem + kAccCol + acc * BN;
+                const int nk = w.kb1 - w.kb0;
+                for (int j = 0; j < nk; ++j) {
+                    const int kb = w.kb0 + (j + w.rot) % nk;
                     if (*abort_flag || !mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
+                    if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
+                    const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
+                    const uint64_t b_desc = b_desc0 + stage * (C_::B_BYTES >> 4);
+                    const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
+                    const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
                     const int g_first = kb * C_::G;
-                    const int g_count = min(C_::G, p.sf_groups - g_first);
-                    const uint32_t sf_col = tmem + kSfCol + stage * C_::SF_COLS_STAGE;
-                    // scale tiles -> TMEM: SFA group g at sf_col + 4g;
-                    // SFB group g, row-tile t at sf_col + SF_COLS_A + 4(g*SFB_TILES + t)
-                    for (int g = 0; g < g_count; ++g) {
-                        const uint32_t sa = smem_u32(smem + C_::OFF_SFA + stage * C_::SFA_BYTES + g * 512);
-                        tc_cp_32x128b_warpx4(sf_col + 4 * g, smem_desc(sa, 0, 128, 0));
-                        for (int t = 0; t < C_::SFB_TILES; ++t) {
-                            const uint32_t sb =
-                                smem_u32(smem + C_::OFF_SFB + stage * C_::SFB_BYTES + t * C_::G * 512 + g * 512);
-                            tc_cp_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (g * C_::SFB_TILES + t),
-                                                 smem_desc(sb, 0, 128, 0));
-                        }
-                    }
-                    const uint32_t a_base = smem_u32(smem + C_::OFF_A + stage * C_::A_BYTES);
-                    const uint32_t b_base = smem_u32(smem + C_::OFF_B + stage * C_::B_BYTES);
                     // valid MMAs in this stage (ragged K): each consumes 32 bytes of K
-                    const int64_t k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
-                    const int64_t k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
-                    const int64_t rem = (int64_t)p.K - (int64_t)kb * k_elem_per_stage;
-                    const int64_t need = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
-                    const int n_mma = need < kMmaPerStage ? (int)need : kMmaPerStage;
-                    for (int i = 0; i < n_mma; ++i) {
-                        const uint64_t adesc = smem_desc(a_base + i * 32, 0, 1024, 2);
-                        const uint64_t bdesc = smem_desc(b_base + i * 32, 0, 1024, 2);
-                        int g, sf_id;
-                        if (KIND == KIND_F4) {
-                            g = i >> 1;           // MMA i covers blocks 2i, 2i+1 of the stage
-                            sf_id = (i & 1) * 2;
-                        } else {
-                            g = 0;                // MMA i covers block i of the stage
-                            sf_id = i;
+                    const int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
+                    const int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
+                    const int rem = p.K - kb * k_elem_per_stage;
+                    if (rem >= k_elem_per_stage) {
+                        // full stage: everything unrolled.
+                        // scale tiles -> TMEM: SFA group g at sf_col + 4g;
+                        // SFB group g, row-tile t at sf_col + SF_COLS_A + 4(g*SFB_TILES + t)
+#pragma unroll
+                        for (int g = 0; g < C_::G; ++g) {
+                            tc_cp_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
+#pragma unroll
+                            for (int t = 0; t < C_::SFB_TILES; ++t)
+                                tc_cp_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (g * C_::SFB_TILES + t),
+                                                     sfb_desc + (t * C_::G + g) * 32);
                         }
-                        const uint32_t idesc = p.idesc | ((uint32_t)sf_id << 4) | ((uint32_t)sf_id << 29);
-                        const uint32_t sfa = sf_col + 4 * g;
-                        const uint32_t sfb = sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES;
-                        const uint32_t acc = (kb > w.kb0 || i > 0) ? 1u : 0u;
-                        if (KIND == KIND_F4)
-                            mma_mxf4(tmem + kAccCol, adesc, bdesc, idesc, sfa, sfb, acc);
-                        else
-                            mma_mxf8f6f4(tmem + kAccCol, adesc, bdesc, idesc, sfa, sfb, acc);
+#pragma unroll
+                        for (int i = 0; i < kMmaPerStage; ++i) {
+                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                            const uint32_t accum = (j > 0 || i > 0) ? 1u : 0u;
+                            if (KIND == KIND_F4)
+                                mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                         sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
+                            else
+                                mma_mxf8f6f4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                             sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
+                        }
+                    } else {
+                        // the ragged last stage of K
+                        const int g_count = min(C_::G, p.sf_groups - g_first);
+                        for (int g = 0; g < g_count; ++g) {
+                            tc_cp_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
+                            for (int t = 0; t < C_::SFB_TILES; ++t)
+                                tc_cp_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (g * C_::SFB_TILES + t),
+                                                     sfb_desc + (t * C_::G + g) * 32);
+                        }
+                        const int n_mma = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
+                        for (int i = 0; i < n_mma; ++i) {
+                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                            const uint32_t accum = (j > 0 || i > 0) ? 1u : 0u;
+                            if (KIND == KIND_F4)
+                                mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                         sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
+                            else
+                                mma_mxf8f6f4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                             sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
+                        }
                     }
                     tc_commit(&empty[stage]);  // stage free once these MMAs have read it
                     if (++stage == STAGES) {
@@ -300,8 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                tc_commit(tmem_full);
-                acc_phase ^= 1;
+                tc_commit(&tmem_full[acc]);
             }
             // every tcgen05 op issued by this thread completes before TMEM is freed
             tc_commit(mma_done);
@@ -310,12 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may read
-        uint8_t* stage_buf = smem + C_::OFF_EPI + (warp - 2) * 2 * C_::EPI_BUF;
-        uint32_t acc_phase = 0;
-        int nbuf = 0;  // chunks issued so far by this warp (buffer = nbuf & 1)
+        uint8_t* stage_buf = smem + C_::OFF_EPI + (warp - 2) * C_::NBUF * C_::EPI_BUF;
+        (void)stage_buf;
+        int nbuf = 0;  // chunks issued so far by this warp (buffer = nbuf % NBUF)
         Work w;
         for (int it = 0; get_work(p, it, w); ++it) {
-            bool ok = !*abort_flag && mbar_wait(tmem_full, acc_phase, p.wait_limit_ns, err);
+            const int acc = it % ACC;
+            const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
+            bool ok = !*abort_flag && mbar_wait(&tmem_full[acc], acc_phase, p.wait_limit_ns, err);
             if (!ok) {
                 *abort_flag = 1;
                 break;
@@ -323,8 +390,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int32_t p0 = w.tp * kBlockM + 32 * q;  // first MMA-A row of this warp
             const int32_t q0 = w.tq * BN;
-            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + kAccCol;
-            if (SWAP) {
+            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + kAccCol + acc * BN;
+            if constexpr (C_::EPI_WARPS == 8) {
+                // this warp: rows p0..p0+31, columns h*128 .. h*128+127 of the tile
+                const int h = (warp - 2) >> 2;
+                uint32_t r[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_row + h * 128 + 32 * c, r[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmem_empty[acc]);  // TMEM free: next tile may start
+                const int32_t pr = p0 + lane;
+                const int32_t qc = q0 + h * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (qc + 32 * c >= p.Q) break;
+                    if (p.epi_red_v4) {
+                        if (pr < p.P) {
+                            float* row = p.C + (int64_t)pr * p.ldc + qc + 32 * c;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (qc + 32 * c + 4 * j + 3 < p.Q) {
+                                    red_add_v4(row + 4 * j, __uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
+                                               __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (qc + 32 * c + 4 * j + e < p.Q) atomicAdd(row + 4 * j + e, __uint_as_float(r[c][4 * j + e]));
+                                }
+                            }
+                        }
+                    } else if (p.use_tma_epi) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            if (qc + 32 * c + 16 * hh >= p.Q) break;
+                            uint8_t* buf = stage_buf;  // one 32 x 16 buffer per warp
+                            if (nbuf >= 1 && lane == 0) bulk_wait_group_read<0>();
+                            __syncwarp();
+                            // [32 rows][16 f32], 64-byte swizzle: 16-B chunk j of row i at j ^ ((i >> 1) & 3)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int js = j ^ ((lane >> 1) & 3);
+                                const uint32_t* v = &r[c][16 * hh + 4 * j];
+                                *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_reduce_add_2d(&tm_c, buf, qc + 32 * c + 16 * hh, p0);
+                                bulk_commit_group();
+                            }
+                            ++nbuf;
+                        }
+                    } else if (pr < p.P) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (qc + 32 * c + j < p.Q) atomicAdd(p.C + (int64_t)pr * p.ldc + qc + 32 * c + j, __uint_as_float(r[c][j]));
+                    }
+                }
+            } else if (SWAP) {
                 // lane i holds acc(p0 + i, q0 + j), j < BN  ->  C[q0 + j][p0 + i]
                 uint32_t r[BN];
 #pragma unroll
@@ -337,10 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tmem_empty);
+                if (lane == 0) mbar_arrive(&tmem_empty[acc]);
                 if (p.use_tma_epi) {
-                    uint8_t* buf = stage_buf + (nbuf & 1) * C_::EPI_BUF;
-                    if (nbuf >= 2 && lane == 0) bulk_wait_group_read<1>();
+                    uint8_t* buf = stage_buf + (nbuf % C_::NBUF) * C_::EPI_BUF;
+                    if (nbuf >= C_::NBUF && lane == 0) bulk_wait_group_read<C_::NBUF - 1>();
                     __syncwarp();
                     float* f = reinterpret_cast<float*>(buf);
 #pragma unroll
@@ -361,46 +486,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                const int nchunks = BN / 16;
+                constexpr int nchunks = BN / 32;
                 const int32_t pr = p0 + lane;
                 for (int c = 0; c < nchunks; ++c) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(t_row + 16 * c, r);
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + 32 * c, r);
                     tmem_ld_wait();
                     if (c == nchunks - 1) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(tmem_empty);
+                        if (lane == 0) mbar_arrive(&tmem_empty[acc]);
                     }
-                    if (q0 + 16 * c >= p.Q) continue;  // chunk wholly past N
+                    if (q0 + 32 * c >= p.Q) continue;  // chunk wholly past N
                     if (p.use_tma_epi) {
-                        uint8_t* buf = stage_buf + (nbuf & 1) * C_::EPI_BUF;
-                        if (nbuf >= 2 && lane == 0) bulk_wait_group_read<1>();
+                        uint8_t* buf = stage_buf + (nbuf % C_::NBUF) * C_::EPI_BUF;
+                        if (nbuf >= C_::NBUF && lane == 0) bulk_wait_group_read<C_::NBUF - 1>();
                         __syncwarp();
-                        // [32 rows][16 f32] with the 64-byte swizzle: 16-B chunk j of
-                        // row i sits at chunk j ^ ((i >> 1) & 3)
+                        // [32 rows][32 f32] with the 128-byte swizzle: 16-B chunk j of
+                        // row i sits at chunk j ^ (i & 7)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int js = j ^ ((lane >> 1) & 3);
+                        for (int j = 0; j < 8; ++j) {
+                            const int js = j ^ (lane & 7);
                             uint4 v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                            *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = v;
+                            *reinterpret_cast<uint4*>(buf + lane * 128 + js * 16) = v;
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_reduce_add_2d(&tm_c, buf, q0 + 16 * c, p0);
+                            tma_reduce_add_2d(&tm_c, buf, q0 + 32 * c, p0);
                             bulk_commit_group();
                         }
                         ++nbuf;
                     } else if (pr < p.P) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (q0 + 16 * c + j < p.Q)
-                                atomicAdd(p.C + (int64_t)pr * p.ldc + q0 + 16 * c + j, __uint_as_float(r[j]));
+                        for (int j = 0; j < 32; ++j)
+                            if (q0 + 32 * c + j < p.Q)
+                                atomicAdd(p.C + (int64_t)pr * p.ldc + q0 + 32 * c + j, __uint_as_float(r[j]));
                     }
                 }
             }
-            acc_phase ^= 1;
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -464,7 +588,7 @@ bool make_operand_map(CUtensorMap* m, const void* codes, int64_t rows, int64_t K
 }
 
 // Tensor map over C (rows x cols f32, row-major) for the reduce-add epilogue.
-bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_cols, int box_rows, bool swz64) {
+bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_cols, int box_rows, int swizzle) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -472,7 +596,9 @@ bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_co
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                    : (swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -494,18 +620,18 @@ uint32_t make_idesc(int kind, int a_fmt, int b_fmt, int n) {
     return d;
 }
 
-template <int KIND, int BN, int STAGES, int SWAP>
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p, int grid,
                 cudaStream_t st) {
-    using C_ = Cfg<KIND, BN, STAGES, SWAP>;
-    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP>;
+    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_>;
+    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_>;
     static int configured_for = -1;  // per-instantiation attribute (process-wide; one value for all devices)
     if (configured_for != C_::SMEM) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM);
         if (e != cudaSuccess) return e;
         configured_for = C_::SMEM;
     }
-    kern<<<grid, kThreads, C_::SMEM, st>>>(ta, tb, tc, p);
+    kern<<<grid, C_::THREADS, C_::SMEM, st>>>(ta, tb, tc, p);
     return cudaGetLastError();
 }
 
@@ -550,7 +676,7 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     if (swap) {
         bn = (int)round_up(Q, 16);  // 16..64
     } else {
-        bn = Q <= 128 ? 128 : 256;
+        bn = Q > 128 ? 256 : 128;
     }
 
     auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
@@ -563,7 +689,9 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     const bool tma_epi = (a.N % 4) == 0;
     std::memset(&tc, 0, sizeof(tc));
     if (tma_epi) {
-        bool okc = swap ? make_c_map(&tc, a.C, a.M, a.N, 32, bn, false) : make_c_map(&tc, a.C, a.M, a.N, 16, 32, true);
+        bool okc = swap         ? make_c_map(&tc, a.C, a.M, a.N, 32, bn, 0)
+                   : bn == 256 ? make_c_map(&tc, a.C, a.M, a.N, 16, 32, 64)
+                               : make_c_map(&tc, a.C, a.M, a.N, 32, 32, 128);
         if (!okc) {
             *detail = "cuTensorMapEncodeTiled rejected C";
             return cudaErrorInvalidValue;
@@ -583,6 +711,8 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     p.idesc = make_idesc(kind, x_fmt, y_fmt, bn);
     p.swap = swap ? 1 : 0;
     p.use_tma_epi = tma_epi ? 1 : 0;
+    p.epi_red_v4 = 0;  // TMA reduce-add measured faster than vector reductions on GB300
+    p.k_rotate = 0;    // K-loop rotation measured no gain
     p.C = a.C;
     p.ldc = a.N;
     p.sfa = x_sf;
@@ -618,10 +748,10 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
         }
     }
     if (kind == KIND_F4) {
-        if (bn == 128) MX_RUN(KIND_F4, 128, 6, 0);
+        if (bn == 128) MX_RUN(KIND_F4, 128, 4, 0);
         MX_RUN(KIND_F4, 256, 4, 0);
     }
-    if (bn == 128) MX_RUN(KIND_F8F6F4, 128, 6, 0);
+    if (bn == 128) MX_RUN(KIND_F8F6F4, 128, 4, 0);
     MX_RUN(KIND_F8F6F4, 256, 4, 0);
 #undef MX_RUN
 }

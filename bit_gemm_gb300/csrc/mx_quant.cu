@@ -25,7 +25,8 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 4;   // independent items per thread in flight (memory-level parallelism)
+constexpr int kMinBlocks = 4; // 4 x 256 threads per SM: at most 64 registers per thread
 
 // ------------------------------------------------------------------ loads
 
@@ -60,31 +61,39 @@ struct Load8<__nv_bfloat16> {
 };
 
 // ------------------------------------------------------------ element round
+//
+// y = |x| * 2^-e is formed by one exact binary32 multiply (a power of two;
+// it also normalizes subnormal inputs), then rounded with integer operations
+// on the bits of y.  Every rule below rounds ties to the LOWER magnitude
+// (the first-index argmin of "Reference encode and decode").
 
-// E2M1: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6} to y >= 0, ties to the lower
-// magnitude, saturating at 6.  The index is the number of midpoints strictly
-// below y.
-__device__ __forceinline__ uint32_t round_e2m1(float y) {
-    return (uint32_t)(y > 0.25f) + (uint32_t)(y > 0.75f) + (uint32_t)(y > 1.25f) + (uint32_t)(y > 1.75f) +
-           (uint32_t)(y > 2.5f) + (uint32_t)(y > 3.5f) + (uint32_t)(y > 5.0f);
+// E4M3FN, y in [2^-6, 512): keep 3 mantissa bits rounding the 20 dropped bits
+// half-down (add 2^19 - 1, truncate; a carry moves into the exponent as it
+// should), re-bias the exponent 127 -> 7 (subtract 120 << 23), and read the
+// 7-bit code from bits 20..26 -- one add and one shift -- then saturate at
+// 0x7E = 448.
+__device__ __forceinline__ uint32_t e4m3_normal_code(uint32_t ybits) {
+    return min((ybits + (0x7FFFFu - 0x3C000000u)) >> 20, 0x7Eu);
 }
 
-// E4M3FN: nearest finite magnitude to y in [0, 512), ties to the lower
-// magnitude, saturating at 448.
-//  * y < 2^-6 (subnormal range, quantum 2^-9): k = ceil(512 y - 1/2) is the
-//    nearest multiple with ties down; k = 8 is the first normal 2^-6, whose
-//    code is also 8.
-//  * otherwise: keep 3 mantissa bits of the binary32 pattern, rounding the 20
-//    dropped bits half-down (add 2^19 - 1, truncate); a carry moves into the
-//    exponent as it should.  Then clamp to 448 and re-bias 127 -> 7.
-__device__ __forceinline__ uint32_t round_e4m3(float y) {
-    if (y < 0.015625f) {
-        const float q = __fsub_rn(__fmul_rn(y, 512.0f), 0.5f);
-        return (uint32_t)__float2int_ru(q) & 0xFu;
-    }
-    uint32_t b = (__float_as_uint(y) + 0x7FFFFu) & 0xFFF00000u;
-    b = b > 0x43E00000u ? 0x43E00000u : b;  // 448 = 1.75 * 2^8
-    return ((((b >> 23) - 120u) << 3) | ((b >> 20) & 7u)) & 0x7Fu;
+// E4M3FN, y in [0, 2^-6): the subnormal quantum is 2^-9, so the code is the
+// nearest integer to 512 y with ties down, ceil(512 y - 1/2).  The fused
+// multiply-add rounds once; the result is exact whenever 512 y >= 1/4, and
+// below that every value rounds into [-1/2, -1/4], whose ceiling is 0.  k = 8
+// is the first normal 2^-6, whose code is also 8.
+__device__ __forceinline__ uint32_t e4m3_subnormal_code(float y) {
+    return (uint32_t)__float2int_ru(__fmaf_rn(y, 512.0f, -0.5f));
+}
+
+// E2M1, y in [0, 8): for y >= 1 keep 1 mantissa bit rounding half-down (add
+// 2^21 - 1), re-bias so that 1.0 is code 2 (subtract 252 << 22), saturate at
+// 7 = 6.0; below 1 the grid is {0, 0.5, 1}, so count the midpoints 0.25 and
+// 0.75 strictly below y.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+    const uint32_t b = __float_as_uint(y);
+    const uint32_t hi = min((b + (0x1FFFFFu - 0x3F000000u)) >> 22, 7u);
+    const uint32_t lo = (uint32_t)(y > 0.25f) + (uint32_t)(y > 0.75f);
+    return y < 1.0f ? lo : hi;
 }
 
 // Quantize the 8 elements a thread owns, given the block's max |bits|.
@@ -110,21 +119,37 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t (&u)[8], uint32_t a
     e = e < -127 ? -127 : (e > 127 ? 127 : e);
     // 2^-e; e <= 125 here, so the pattern is a normal binary32.
     const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+    if (FMT == FMT_E2M1) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t mag = u[i] & 0x7FFFFFFFu;
-        const float y = __fmul_rn(__uint_as_float(mag), inv);  // exact where it matters
-        uint32_t c = FMT == FMT_E2M1 ? round_e2m1(y) : round_e4m3(y);
-        if ((u[i] >> 31) && mag) c |= kSign;  // x < 0 (not -0.0)
-        code[i] = c;
+        for (int i = 0; i < 8; ++i) {
+            const float y = __fmul_rn(__uint_as_float(u[i] & 0x7FFFFFFFu), inv);
+            // sign bit when x < 0: the pattern is above 0x80000000 (-0.0 is not)
+            code[i] = e2m1_code(y) | (u[i] > 0x80000000u ? kSign : 0u);
+        }
+    } else {
+        float y[8];
+        bool any_small = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            y[i] = __fmul_rn(__uint_as_float(u[i] & 0x7FFFFFFFu), inv);
+            code[i] = e4m3_normal_code(__float_as_uint(y[i])) | (u[i] > 0x80000000u ? kSign : 0u);
+            any_small |= y[i] < 0.015625f;
+        }
+        if (any_small) {  // rare: some element below 2^-6 (zeros included)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (y[i] < 0.015625f) code[i] = e4m3_subnormal_code(y[i]) | (u[i] > 0x80000000u ? kSign : 0u);
+        }
     }
     return (uint32_t)(e + 127);
 }
 
 template <typename InT, int FMT, int LAYOUT>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const InT* __restrict__ x, int64_t nblocks, int64_t nb,
+__global__ void __launch_bounds__(kThreads, kMinBlocks) quantize_kernel(const InT* __restrict__ x, int64_t nblocks, int64_t nb,
                                                             int64_t rows, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ scales) {
+    // 64 bytes of input in flight per thread: 4 items of bf16, 2 of f32
+    constexpr int kU = sizeof(InT) == 2 ? kUnroll : kUnroll / 2;
     const int lane = threadIdx.x & 31;
     const int part = lane & 3;  // which 8 of the block's 32 elements
     const int64_t nthreads = nblocks * 4;
@@ -132,10 +157,10 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const InT* __restric
     const int64_t nb4 = round_up(nb, 4);
 
     for (int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; t0 - lane < nthreads;
-         t0 += stride * kUnroll) {
-        uint32_t u[kUnroll][8];
+         t0 += stride * kU) {
+        uint32_t u[kU][8];
 #pragma unroll
-        for (int q = 0; q < kUnroll; ++q) {
+        for (int q = 0; q < kU; ++q) {
             const int64_t t = t0 + q * stride;
             if (t < nthreads) {
                 Load8<InT>::run(x + t * 8, u[q]);
@@ -145,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const InT* __restric
             }
         }
 #pragma unroll
-        for (int q = 0; q < kUnroll; ++q) {
+        for (int q = 0; q < kU; ++q) {
             const int64_t t = t0 + q * stride;
             if (t - lane >= nthreads) break;  // warp-uniform: whole warp past the end
             uint32_t m = 0;
@@ -159,9 +184,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const InT* __restric
             const int64_t b = t >> 2;  // block index
             if (valid) {
                 if (FMT == FMT_E2M1) {
-                    uint32_t w = 0;
+                    uint32_t w = c[7];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) w |= c[i] << (4 * i);  // element 0 in the low nibble
+                    for (int i = 6; i >= 0; --i) w = w * 16u + c[i];  // element 0 in the low nibble
                     __stcs(reinterpret_cast<uint32_t*>(codes) + t, w);
                 } else {
                     uint2 w;
@@ -219,72 +244,108 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const InT* __restric
 
 // --------------------------------------------------------------- dequantize
 
-// E2M1 magnitude index (3 bits) -> binary32 bits of the magnitude.
-__device__ __forceinline__ uint32_t e2m1_bits(uint32_t c) {
-    const uint32_t E = (c >> 1) & 3u, M = c & 1u;
-    if (E == 0) return M ? 0x3F000000u : 0u;  // 0.5 * M
-    return ((E + 126u) << 23) | (M << 22);    // 2^(E-1) * (1 + M/2)
-}
-
-// E4M3FN code (7 bits) -> binary32 bits of the magnitude; 0x7F is NaN.
-__device__ __forceinline__ uint32_t e4m3_bits(uint32_t c) {
-    const uint32_t E = c >> 3, M = c & 7u;
-    if (c == 0x7Fu) return 0x7FC00000u;
-    if (E == 0) return __float_as_uint((float)M * 0.001953125f);  // M * 2^-9
-    return ((E + 120u) << 23) | (M << 20);                        // 2^(E-7) * (1 + M/8)
+// Decoding assembles binary32 bits directly.
+//  E4M3FN normal (exponent field E >= 1): 2^(E-7) (1 + M/8) has the bits
+//    (E + 120) << 23 | M << 20 = (code7 << 20) + (120 << 23).
+//  E4M3FN subnormal (E = 0): M * 2^-9, exact in binary32.  Code 0x7F is NaN.
+//  E2M1 (E >= 1): 2^(E-1) (1 + M/2) has the bits (code3 << 22) + (126 << 23);
+//    for E = 0 the same assembly with exponent 127 gives 1 + M/2, and 1.0 is
+//    subtracted afterwards (0 and 0.5).
+__device__ __forceinline__ float e4m3_decode_slow(uint32_t c) {
+    const uint32_t c7 = c & 0x7Fu;
+    float m;
+    if (c7 == 0x7Fu) m = __uint_as_float(0x7FC00000u);
+    else if (c7 < 8u) m = (float)c7 * 0.001953125f;
+    else m = __uint_as_float((c7 << 20) + 0x3C000000u);
+    return (c & 0x80u) ? -m : m;
 }
 
 template <int FMT, int LAYOUT>
-__global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
-                                                              const uint8_t* __restrict__ scales, int64_t nblocks,
-                                                              int64_t nb, float* __restrict__ y) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                                          const uint8_t* __restrict__ scales,
+                                                                          int64_t nblocks, int64_t nb,
+                                                                          float* __restrict__ y) {
     const int64_t nthreads = nblocks * 4;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const int64_t nb4 = round_up(nb, 4);
-    for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < nthreads; t += stride) {
-        const int64_t b = t >> 2;
-        int64_t soff;
-        if (LAYOUT == LAYOUT_ROWMAJOR) {
-            soff = b;
-        } else {
-            const int64_t r = b / nb, j = b - r * nb;
-            soff = mma_scale_offset(r, j, nb4);
-        }
-        const uint32_t s = __ldg(scales + soff);
-        uint32_t c[8];
-        if (FMT == FMT_E2M1) {
-            const uint32_t w = __ldcs(reinterpret_cast<const uint32_t*>(codes) + t);
+    for (int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; t0 < nthreads; t0 += stride * kUnroll) {
+        // issue every load of this round first, then decode and store
+        uint2 w[kUnroll];
+        uint32_t sc[kUnroll];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) c[i] = (w >> (4 * i)) & 0xFu;
-        } else {
-            const uint2 w = __ldcs(reinterpret_cast<const uint2*>(codes) + t);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                c[i] = (w.x >> (8 * i)) & 0xFFu;
-                c[4 + i] = (w.y >> (8 * i)) & 0xFFu;
+        for (int q = 0; q < kUnroll; ++q) {
+            const int64_t t = t0 + q * stride;
+            w[q] = make_uint2(0, 0);
+            sc[q] = 0;
+            if (t < nthreads) {
+                const int64_t b = t >> 2;
+                int64_t soff;
+                if (LAYOUT == LAYOUT_ROWMAJOR) {
+                    soff = b;
+                } else {
+                    const int64_t r = b / nb, j = b - r * nb;
+                    soff = mma_scale_offset(r, j, nb4);
+                }
+                sc[q] = __ldg(scales + soff);
+                if (FMT == FMT_E2M1)
+                    w[q].x = __ldcs(reinterpret_cast<const uint32_t*>(codes) + t);
+                else
+                    w[q] = __ldcs(reinterpret_cast<const uint2*>(codes) + t);
             }
         }
-        // 2^(s-127) as binary32 (s = 0 is the subnormal 2^-127).
-        const float scale = s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
-        float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t mbits, sign;
+        for (int q = 0; q < kUnroll; ++q) {
+            const int64_t t = t0 + q * stride;
+            if (t >= nthreads) break;
+            const uint32_t s = sc[q];
+            uint32_t c[8];
             if (FMT == FMT_E2M1) {
-                mbits = e2m1_bits(c[i] & 7u);
-                sign = (c[i] & 8u) << 28;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c[i] = (w[q].x >> (4 * i)) & 0xFu;
             } else {
-                mbits = e4m3_bits(c[i] & 0x7Fu);
-                sign = (c[i] & 0x80u) << 24;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    c[i] = (w[q].x >> (8 * i)) & 0xFFu;
+                    c[4 + i] = (w[q].y >> (8 * i)) & 0xFFu;
+                }
             }
-            // Exact: at most 4 significant bits times a power of two (or an
-            // IEEE overflow to infinity, as the definition gives).
-            v[i] = __fmul_rn(__uint_as_float(mbits | sign), scale);
-            if (s == 0xFFu) v[i] = __uint_as_float(0x7FC00000u);  // NaN scale poisons the block
+            // 2^(s-127) as binary32 (s = 0 is the subnormal 2^-127); the NaN scale
+            // 0xFF becomes a NaN multiplier, which poisons the whole block.
+            const float scale = s == 0xFFu ? __uint_as_float(0x7FC00000u)
+                                           : (s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u));
+            float v[8];
+            if (FMT == FMT_E2M1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t m22 = (c[i] & 7u) << 22;
+                    const bool sub = m22 < (2u << 22);
+                    const uint32_t mag = m22 + (sub ? 0x3F800000u : 0x3F000000u);
+                    // exact: the true magnitude is representable and the fma rounds
+                    // once; the sign bit goes in afterwards so code 0x8 gives -0.0
+                    const float m = __fmaf_rn(__uint_as_float(mag), scale, sub ? -scale : 0.0f);
+                    v[i] = __uint_as_float(__float_as_uint(m) | ((c[i] & 8u) << 28));
+                }
+            } else {
+                // fast path unless some code is subnormal (exponent field 0) or NaN
+                const uint32_t w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+                const uint32_t w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+                const uint32_t slow = __vcmpeq4(w0 & 0x78787878u, 0u) | __vcmpeq4(w0 & 0x7F7F7F7Fu, 0x7F7F7F7Fu) |
+                                      __vcmpeq4(w1 & 0x78787878u, 0u) | __vcmpeq4(w1 & 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                if (slow == 0u) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t bits = ((c[i] & 0x7Fu) << 20) + 0x3C000000u + ((c[i] & 0x80u) << 24);
+                        v[i] = __fmul_rn(__uint_as_float(bits), scale);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(e4m3_decode_slow(c[i]), scale);
+                }
+            }
+            float4* out = reinterpret_cast<float4*>(y) + t * 2;
+            __stcs(out, make_float4(v[0], v[1], v[2], v[3]));
+            __stcs(out + 1, make_float4(v[4], v[5], v[6], v[7]));
         }
-        float4* out = reinterpret_cast<float4*>(y) + t * 2;
-        __stcs(out, make_float4(v[0], v[1], v[2], v[3]));
-        __stcs(out + 1, make_float4(v[4], v[5], v[6], v[7]));
     }
 }
 
@@ -324,7 +385,8 @@ template <typename InT, int FMT>
 cudaError_t quant_dispatch_layout(const InT* x, int64_t nblocks, int64_t nb, int64_t rows, uint8_t* codes,
                                   uint8_t* scales, int layout, cudaStream_t st) {
     const int64_t work = nblocks * 4;
-    int64_t grid = grid_for((work + kUnroll - 1) / kUnroll, 8);
+    constexpr int kU = sizeof(InT) == 2 ? kUnroll : kUnroll / 2;
+    int64_t grid = grid_for((work + kU - 1) / kU, kMinBlocks);
     if (layout == LAYOUT_MMA) {
         const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
         const int64_t g2 = grid_for(pad, 8);
@@ -359,7 +421,7 @@ cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t 
                               int layout, float* y, cudaStream_t st) {
     const int64_t nb = cols / 32;
     const int64_t nblocks = rows * nb;
-    const unsigned grid = (unsigned)grid_for(nblocks * 4, 8);
+    const unsigned grid = (unsigned)grid_for((nblocks * 4 + kUnroll - 1) / kUnroll, kMinBlocks);
     const uint8_t* c = static_cast<const uint8_t*>(codes);
     if (fmt == FMT_E2M1) {
         if (layout == LAYOUT_MMA)
