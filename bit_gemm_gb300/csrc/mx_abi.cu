@@ -178,6 +178,9 @@ mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_for
     const bool mixed = a_fmt != b_fmt;
     if (mixed && K % 128)
         return fail(MX_ERR_SHAPE, "mixed E2M1/E4M3FN operands need K %% 128 == 0 (K = %lld)", (long long)K);
+    if (scale_layout == MX_SCALES_ROWMAJOR && K % 128)
+        return fail(MX_ERR_SHAPE, "row-major scales need K %% 128 == 0 (K = %lld); use MX_SCALES_MMA",
+                    (long long)K);
     if (M == 0 || N == 0 || K == 0) return ok();  // C += (empty sum) is C
     if (!a_codes || !a_scales || !b_codes || !b_scales || !C)
         return fail(MX_ERR_NULL, "operand pointers must be non-NULL");

@@ -81,6 +81,8 @@ struct GemmParams {
     const uint8_t* sfa;    // scales of the MMA A operand (tensor-core layout)
     const uint8_t* sfb;    // scales of the MMA B operand
     uint32_t tx_a, tx_b;   // bytes one stage's code load counts on its barrier
+    int32_t sf_rowmajor;   // 1: scales are row-major [rows][K/32]; gathered by the producer lanes
+    int32_t nb;            // K / 32 (row stride of row-major scales, a multiple of 4)
 };
 
 struct Work {
@@ -187,7 +189,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // row-major scales: the 32 producer lanes' cp.async arrivals as well
+            mbar_init(&full[s], p.sf_rowmajor ? 33 : 1);
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < ACC; ++a) {
@@ -212,54 +215,87 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
-            uint32_t issued_phase = 0;
-            bool ok = true;
-            Work w;
-            for (int it = 0; ok && get_work(p, it, w); ++it) {
-                const int32_t p0 = w.tp * kBlockM;
-                const int32_t q0 = w.tq * BN;
-                const int nk = w.kb1 - w.kb0;
-                for (int j = 0; j < nk; ++j) {
-                    const int kb = w.kb0 + (j + w.rot) % nk;
-                    if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err)) {
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    // scale groups present for this stage (the last stage of a
-                    // ragged K may need only the first)
-                    const int g_first = kb * C_::G;
-                    const int g_count = min(C_::G, p.sf_groups - g_first);
-                    // scale row-tiles covering rows [q0, q0 + BN), clipped to the tensor
-                    const int sfb_tiles = min(C_::SFB_TILES, (p.Q + 127) / 128 - (q0 >> 7));
-                    const uint32_t bytes = p.tx_a + p.tx_b + g_count * 512 + sfb_tiles * g_count * 512;
+        // Lane 0 issues the TMA loads; with row-major scales every lane also
+        // gathers 4-byte scale words of its rows straight into the tensor-core
+        // tile layout (row r -> line r % 32, word (r / 32) % 4 of its tile).
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
+        uint32_t issued_phase = 0;
+        bool ok = true;
+        Work w;
+        for (int it = 0; ok && get_work(p, it, w); ++it) {
+            const int32_t p0 = w.tp * kBlockM;
+            const int32_t q0 = w.tq * BN;
+            const int nk = w.kb1 - w.kb0;
+            for (int j = 0; j < nk; ++j) {
+                const int kb = w.kb0 + (j + w.rot) % nk;
+                int okw = 1;
+                if (lane == 0) okw = !*abort_flag && mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
+                okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                if (!okw) {
+                    if (lane == 0) *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                // scale groups present for this stage (the last stage of a
+                // ragged K may need only the first)
+                const int g_first = kb * C_::G;
+                const int g_count = min(C_::G, p.sf_groups - g_first);
+                // scale row-tiles covering rows [q0, q0 + BN), clipped to the tensor
+                const int sfb_tiles = min(C_::SFB_TILES, (p.Q + 127) / 128 - (q0 >> 7));
+                if (lane == 0) {
+                    const uint32_t bytes = p.tx_a + p.tx_b +
+                                           (p.sf_rowmajor ? 0u : (uint32_t)(g_count * 512 + sfb_tiles * g_count * 512));
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     tma_load_2d(smem + C_::OFF_A + stage * C_::A_BYTES, &tm_a, kb * kRowBytes, p0, &full[stage]);
                     tma_load_2d(smem + C_::OFF_B + stage * C_::B_BYTES, &tm_b, kb * kRowBytes, q0, &full[stage]);
-                    const uint8_t* sa = p.sfa + ((int64_t)w.tp * p.sf_groups + g_first) * 512;
-                    bulk_load(smem + C_::OFF_SFA + stage * C_::SFA_BYTES, sa, g_count * 512, &full[stage]);
-                    for (int t = 0; t < sfb_tiles; ++t) {
-                        const uint8_t* sb = p.sfb + ((int64_t)((q0 >> 7) + t) * p.sf_groups + g_first) * 512;
-                        bulk_load(smem + C_::OFF_SFB + stage * C_::SFB_BYTES + t * C_::G * 512, sb,
-                                  g_count * 512, &full[stage]);
-                    }
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
+                    if (!p.sf_rowmajor) {
+                        const uint8_t* sa = p.sfa + ((int64_t)w.tp * p.sf_groups + g_first) * 512;
+                        bulk_load(smem + C_::OFF_SFA + stage * C_::SFA_BYTES, sa, g_count * 512, &full[stage]);
+                        for (int t = 0; t < sfb_tiles; ++t) {
+                            const uint8_t* sb = p.sfb + ((int64_t)((q0 >> 7) + t) * p.sf_groups + g_first) * 512;
+                            bulk_load(smem + C_::OFF_SFB + stage * C_::SFB_BYTES + t * C_::G * 512, sb,
+                                      g_count * 512, &full[stage]);
+                        }
                     }
                 }
+                if (p.sf_rowmajor) {
+                    for (int g = 0; g < g_count; ++g) {
+                        const int64_t word = 4 * (int64_t)(g_first + g);  // byte offset of the group in a row
+                        uint8_t* da = smem + C_::OFF_SFA + stage * C_::SFA_BYTES + g * 512 + lane * 16;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int32_t r = p0 + lane + 32 * i;
+                            const int32_t rc = r < p.P ? r : p.P - 1;
+                            cp_async_4(da + 4 * i, p.sfa + (int64_t)rc * p.nb + word, r < p.P ? 4u : 0u);
+                        }
+                        for (int t = 0; t < C_::SFB_TILES; ++t) {
+                            uint8_t* db = smem + C_::OFF_SFB + stage * C_::SFB_BYTES + (t * C_::G + g) * 512 + lane * 16;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int32_t r = q0 + 128 * t + lane + 32 * i;
+                                const int32_t rc = r < p.Q ? r : p.Q - 1;
+                                cp_async_4(db + 4 * i, p.sfb + (int64_t)rc * p.nb + word, r < p.Q ? 4u : 0u);
+                            }
+                        }
+                    }
+                    cp_async_arrive_noinc(&full[stage]);
+                }
+                issued_mask |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
             }
-            if (!ok) {
-                // drain: wait (bounded) for our own loads still in flight
+        }
+        if (!ok) {
+            // drain: wait (bounded) for our own loads still in flight
+            if (p.sf_rowmajor) cp_async_wait_all();
+            if (lane == 0)
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, p.wait_limit_ns, err);
-            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
@@ -304,6 +340,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                         break;
                     }
                     tc_fence_after();
+                    // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
+                    // through the async proxy
+                    if (p.sf_rowmajor) fence_proxy_async_smem();
                     const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
                     if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
                     const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
@@ -350,12 +389,14 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                         const int n_mma = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
                         for (int i = 0; i < n_mma; ++i) {
                             const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                            const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
+                            const uint32_t id = p.idesc | (sf_id << 4) | (sf_id << 29);
                             const uint32_t accum = (j > 0 || i > 0) ? 1u : 0u;
                             if (KIND == KIND_F4)
-                                mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
                                          sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
                             else
-                                mma_mxf8f6f4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                mma_mxf8f6f4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
                                              sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
                         }
                     }
@@ -665,10 +706,6 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     const int y_fmt = swap ? a.a_fmt : a.b_fmt;
     const int64_t Q = swap ? a.M : a.N;
 
-    if (a.scale_layout != LAYOUT_MMA) {
-        *detail = "row-major scales are not accepted by block_matmul yet; use MX_SCALES_MMA or mx_scales_relayout";
-        return cudaErrorNotSupported;
-    }
     const int kind = (x_fmt == FMT_E2M1 && y_fmt == FMT_E2M1) ? KIND_F4 : KIND_F8F6F4;
     const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
 
@@ -721,6 +758,8 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     // (16U4_ALIGN16B) completes with the packed byte count: 64 B per row.
     p.tx_a = (uint32_t)kBlockM * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
     p.tx_b = (uint32_t)bn * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.sf_rowmajor = a.scale_layout == LAYOUT_ROWMAJOR ? 1 : 0;
+    p.nb = (int32_t)(a.K / 32);
     const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
     p.total_units = tiles * p.k_stages;
     const int sms = sm_count();

@@ -136,7 +136,8 @@ MX_API mx_status_t mx_dequantize(const void* codes, const uint8_t* scales, int64
  *       format b_fmt) so that it too is blocked along its reduction axis K
  *       ([Dialect] "The block axis": the law is reduction-axis blocking).
  *   scale_layout : layout of both a_scales and b_scales.  MX_SCALES_MMA is the
- *       fast path; MX_SCALES_ROWMAJOR is accepted as well.
+ *       fast path (one bulk copy per scale tile); MX_SCALES_ROWMAJOR is accepted
+ *       when K % 128 == 0 (the kernel gathers 4-byte scale words itself).
  *   C : M x N f32, row-major, read and written in place; must not overlap an
  *       input (MX_ERR_UNSUPPORTED).
  * Formats: any pair of MX_E2M1 / MX_E4M3FN.  Shape rules: K % 32 == 0; when

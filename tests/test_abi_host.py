@@ -111,6 +111,7 @@ def test_block_matmul_validation():
     assert g(C=A16 * 64 + 4) == ALIGN
     assert g(af=mx.E4M3FN, b=A16 * 3 + 16) == ALIGN  # the E2M1 operand of a mixed product needs 32 B
     assert g(C=A16) == UNSUP                    # C overlaps A's codes
+    assert g(layout=mx.SCALES_ROWMAJOR, K=96) == SHAPE   # row-major scales need K % 128 == 0
     assert g(M=0) == OK and g(N=0) == OK and g(K=0) == OK
 
 

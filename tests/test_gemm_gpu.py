@@ -133,6 +133,20 @@ def test_ragged_shapes(M, N, K, fa, fb):
     run_full(randn(rng, (M, K)), randn(rng, (N, K)), fa, fb, randn(rng, (M, N)))
 
 
+# ------------------------------------------------------ row-major scales
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (128, 128, 256, mx.E2M1, mx.E2M1),
+    (200, 300, 384, mx.E4M3FN, mx.E4M3FN),   # ragged M and N: scale rows past the end read as zero
+    (130, 512, 128, mx.E4M3FN, mx.E2M1),
+    (16, 1024, 512, mx.E4M3FN, mx.E2M1),     # swapped operands
+    (256, 512, 8192, mx.E2M1, mx.E2M1),      # split along K across CTAs
+])
+def test_row_major_scales(M, N, K, fa, fb):
+    rng = np.random.default_rng(M + 2 * N + 3 * K)
+    run_full(randn(rng, (M, K)), randn(rng, (N, K)), fa, fb, randn(rng, (M, N)), layout=mx.SCALES_ROWMAJOR)
+
+
 # ------------------------------------------------------- workload 3 (decode)
 
 def test_workload3_decode_full():
