@@ -303,7 +303,7 @@ def bench_e2e(mx, hl, steps, world):
             "h2d_bytes_per_step": rows * cols * 2, "d2h_bytes_per_step": rows * cols * 4, "steps": n}
 
 
-def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0):
+def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0):
     """block_matmul workloads.  Weights are quantized before timing; the step
     includes the activation quantize where the workload quantizes on the fly."""
     w = workloads.make(cfg, scale=scale)
@@ -356,8 +356,9 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0):
 
     step(0)
     mx.mx_device_status()
-    sec = max_over_ranks(timed_graph_steps(step, nsets, steps, warmup, world), world)
-    sec_g = max_over_ranks(timed_graph_steps(gemm_only, nsets, steps, 3, world), world)
+    with ClockSampler(dev_index) as clk:
+        sec = max_over_ranks(timed_graph_steps(step, nsets, steps, warmup, world), world)
+        sec_g = max_over_ranks(timed_graph_steps(gemm_only, nsets, steps, 3, world), world)
     mx.mx_device_status()
     flops = 2.0 * M * N * K
     tf_step = job_throughput(flops * steps, world, sec) / 1e12
@@ -371,10 +372,26 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0):
         "tflops_gemm": tf_gemm, "us_gemm": sec_g / steps * 1e6,
         "tensor_peak_tflops": peak_tf, "tensor_frac": tf_gemm / peak_tf,
         "gemm_gbs": gbs_gemm, "hbm_frac": gbs_gemm / peaks["hbm_gbs"], "gemm_bytes": gemm_bytes,
-        "launches_per_step": 2 if quant_a else 1, "nsets": nsets}
+        "launches_per_step": 2 if quant_a else 1, "nsets": nsets, "clocks": clk.summary()}
     del sets, A, C0, bc, bs
     torch.cuda.empty_cache()
     return out
+
+
+def measured_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernel source has changed since the counters were taken."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "bit_gemm_gb300", "csrc", "mx_quant.cu")
+    if not os.path.exists(prof):
+        return None
+    with open(prof) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != d.get("mx_quant_cu_sha256"):
+            return None
+    return d.get(key)
 
 
 # ---------------------------------------------------------- CPU baseline
@@ -394,14 +411,18 @@ def oracle_step_rate(rows_sample: int, x_full: torch.Tensor, reps: int = 1):
 
 
 def cpu_baseline(x_full: torch.Tensor, target_s: float = 10.0):
+    """The oracle, as it stands, on the host cores: quantize + dequantize of a
+    sample of the headline workload, repeated until about target_s seconds."""
     import oracle
     threads = oracle.num_threads()
     dt, _ = oracle_step_rate(8, x_full)
     per_row = max(dt / 8, 1e-6)
     rows = int(min(x_full.shape[0], max(8, target_s / per_row)))
-    dt, nbytes = oracle_step_rate(rows, x_full)
+    reps = max(1, min(50, int(round(target_s / (per_row * rows)))))
+    dt, nbytes = oracle_step_rate(rows, x_full, reps)
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows} of 4096 rows of the bf16 4096x4096 workload (quantize + dequantize), {dt:.1f} s"}
+            "sample": f"{rows} of 4096 rows of the bf16 4096x4096 workload (quantize + dequantize), "
+                      f"{reps} passes, {dt:.1f} s"}
 
 
 # ------------------------------------------------------------------- main
@@ -472,7 +493,7 @@ def main():
             out = {k: v for k, v in hl.items() if k not in ("x_host",)}
         else:
             cfg = {"decode": 3, "square": 4, "prefill": 5}[args.only]
-            out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale)
+            out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale, dev_index)
         if rank == 0:
             print(json.dumps(out, default=str), flush=True)
         return
@@ -481,17 +502,13 @@ def main():
     gemms = []
     if not args.no_gemm:
         for cfg in (3, 4, 5):
-            gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks))
+            gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks, 1.0, dev_index))
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(hl["x_host"])
 
     dom = hl[hl["dominant"]]
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get(f"{hl['dominant']}_mxfp8_4096")
+    traffic = measured_traffic(f"{hl['dominant']}_mxfp8_4096")
     line = {
         "metric": METRIC, "value": hl["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": hl["ms_per_step"], "higher_is_better": True, "scaling": "weak",

@@ -96,10 +96,42 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
     return y < 1.0f ? lo : hi;
 }
 
-// Quantize the 8 elements a thread owns, given the block's max |bits|.
-// Returns the scale byte; fills 8 codes (sign included).
+// Padding of the tensor-core layout: rows up to a multiple of 128 and blocks
+// per row up to a multiple of 4 are written as 0 (scale 2^-127, finite, so
+// zero-filled operand padding contributes exactly 0).  Grid-strided.
+__device__ __forceinline__ void write_mma_padding(uint8_t* __restrict__ scales, int64_t rows, int64_t nb) {
+    const int64_t nb4 = round_up(nb, 4);
+    const int64_t r128 = round_up(rows, 128);
+    const int64_t pad_rows = (r128 - rows) * nb4;
+    const int64_t pad_cols = rows * (nb4 - nb);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < pad_rows + pad_cols; p += stride) {
+        int64_t r, j;
+        if (p < pad_rows) {
+            r = rows + p / nb4;
+            j = p - (r - rows) * nb4;
+        } else {
+            const int64_t q = p - pad_rows;
+            const int64_t w = nb4 - nb;
+            r = q / w;
+            j = nb + (q - r * w);
+        }
+        scales[mma_scale_offset(r, j, nb4)] = 0;
+    }
+}
+
+// Quantize the 8 elements a thread owns, given the block's max and min
+// |bits|.  Returns the scale byte; fills 8 codes (sign included).
+//
+// Fast path (the block's exponent e >= -120, so every element that reaches
+// the normal code range is itself a normal binary32): dividing by 2^e is a
+// subtraction of e from the exponent field, which folds into the rounding
+// constant -- one add and one shift per element.  The sign of a nonzero
+// element is its bit 31.  Elements below the format's smallest normal (rare;
+// zeros included) and blocks with e < -120 take the exact multiply path.
 template <int FMT>
-__device__ __forceinline__ uint32_t quantize8(const uint32_t (&u)[8], uint32_t amax_bits, uint32_t (&code)[8]) {
+__device__ __forceinline__ uint32_t quantize8(const uint32_t (&u)[8], uint32_t amax_bits, uint32_t amin_bits,
+                                              uint32_t (&code)[8]) {
     constexpr int kEmax = FMT == FMT_E2M1 ? 2 : 8;
     constexpr uint32_t kSign = FMT == FMT_E2M1 ? 0x8u : 0x80u;
     if (amax_bits >= 0x7F800000u) {  // NaN or infinity in the block: poison it
@@ -117,7 +149,23 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t (&u)[8], uint32_t a
     const int E = fe ? fe - 127 : (31 - __clz((int)amax_bits)) - 149;
     int e = E - kEmax;
     e = e < -127 ? -127 : (e > 127 ? 127 : e);
-    // 2^-e; e <= 125 here, so the pattern is a normal binary32.
+    // smallest normal of the element format, as a bound on |x|: 2^-6 * 2^e
+    // (E4M3) or 1.0 * 2^e (E2M1); below it the element takes the slow path
+    const int small_exp = (FMT == FMT_E2M1 ? 0 : -6) + e;
+    const bool fast = e >= -120;
+    const uint32_t small_bits = fast ? (uint32_t)(small_exp + 127) << 23 : 0xFFFFFFFFu;
+    if (fast && FMT == FMT_E4M3 && amin_bits >= small_bits) {
+        // code = round-half-down to 3 mantissa bits of |x| / 2^e, re-biased:
+        // ((bits(|x|) - (e << 23)) + 2^19 - 1 - (120 << 23)) >> 20, saturated at 0x7E
+        const uint32_t k = 0x7FFFFu - 0x3C000000u - ((uint32_t)e << 23);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = u[i] & 0x7FFFFFFFu;
+            code[i] = min((a + k) >> 20, 0x7Eu) | ((u[i] >> 24) & kSign);
+        }
+        return (uint32_t)(e + 127);
+    }
+    // exact multiply path: y = |x| * 2^-e (e <= 125, so 2^-e is a normal binary32)
     const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
     if (FMT == FMT_E2M1) {
 #pragma unroll
@@ -127,29 +175,140 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t (&u)[8], uint32_t a
             code[i] = e2m1_code(y) | (u[i] > 0x80000000u ? kSign : 0u);
         }
     } else {
-        float y[8];
-        bool any_small = false;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            y[i] = __fmul_rn(__uint_as_float(u[i] & 0x7FFFFFFFu), inv);
-            code[i] = e4m3_normal_code(__float_as_uint(y[i])) | (u[i] > 0x80000000u ? kSign : 0u);
-            any_small |= y[i] < 0.015625f;
-        }
-        if (any_small) {  // rare: some element below 2^-6 (zeros included)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (y[i] < 0.015625f) code[i] = e4m3_subnormal_code(y[i]) | (u[i] > 0x80000000u ? kSign : 0u);
+            const float y = __fmul_rn(__uint_as_float(u[i] & 0x7FFFFFFFu), inv);
+            const uint32_t c = y < 0.015625f ? e4m3_subnormal_code(y) : e4m3_normal_code(__float_as_uint(y));
+            code[i] = c | (u[i] > 0x80000000u ? kSign : 0u);
         }
     }
     return (uint32_t)(e + 127);
+}
+
+// bf16 -> E4M3FN, two elements per 32-bit word (the low half is the lower
+// element).  For a block whose exponent e >= -120 and whose elements all lie
+// at or above the E4M3 normal range (|x| >= 2^(e-6)), each half h of a word
+// gives its code as ((h - (e << 7)) + 7 - (120 << 7)) >> 4: subtract e from
+// the bf16 exponent field, round the 4 dropped mantissa bits half-down,
+// re-bias 127 -> 7.  Both halves are formed by one 32-bit add: the low half's
+// carry into the high half is 1 exactly when the constant K is negative, so
+// it is pre-subtracted from the high half of the constant.
+__device__ __forceinline__ uint32_t bf16_pair_e4m3(uint32_t w, uint32_t k2) {
+    const uint32_t t = (w & 0x7FFF7FFFu) + k2;                      // r_lo | r_hi << 16
+    uint32_t c = __vminu2((t >> 4) & 0x00FF00FFu, 0x007E007Eu);      // saturate at 448
+    return c | ((w >> 8) & 0x00800080u);                            // sign bits 15, 31 -> 7, 23
+}
+
+template <int LAYOUT, int kU, int kMB, int kPipe>
+__global__ void __launch_bounds__(kThreads, kMB)
+    quantize_bf16_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int64_t nblocks, int64_t nb, int64_t rows,
+                              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int part = lane & 3;
+    const int64_t nthreads = nblocks * 4;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const int64_t nb4 = round_up(nb, 4);
+    uint4 v[kU], nxt[kPipe ? kU : 1];
+    int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+        const int64_t t = t0 + q * stride;
+        v[q] = t < nthreads ? __ldcs(reinterpret_cast<const uint4*>(x) + t) : make_uint4(0, 0, 0, 0);
+    }
+    for (; t0 - lane < nthreads; t0 += stride * kU) {
+        if (kPipe) {
+            // issue the next round's loads before working on this round
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int64_t t = t0 + (kU + q) * stride;
+                nxt[q % (kPipe ? kU : 1)] = t < nthreads ? __ldcs(reinterpret_cast<const uint4*>(x) + t) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int64_t t = t0 + q * stride;
+            if (t - lane >= nthreads) break;  // warp-uniform
+            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+            // |bits| max and min over the thread's 8 elements, 16 bits per lane
+            uint32_t mx2 = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
+                                    __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+            uint32_t mn2 = __vminu2(__vminu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
+                                    __vminu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+            uint32_t m = max(mx2 & 0xFFFFu, mx2 >> 16);
+            const uint32_t mn16 = min(mn2 & 0xFFFFu, mn2 >> 16);
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            const uint32_t amax_bits = m << 16;  // binary32 pattern of the bf16 amax
+            uint32_t sbyte;
+            uint2 out;
+            // fast path conditions (a finite, nonzero block is required)
+            const int fe = (int)(amax_bits >> 23);
+            int e = (fe ? fe - 127 : (31 - __clz((int)amax_bits)) - 149) - 8;
+            e = e < -127 ? -127 : (e > 127 ? 127 : e);
+            const bool fast = amax_bits - 1u < 0x7F7FFFFFu  // nonzero and finite
+                              && e >= -120 && mn16 >= (uint32_t)(e + 121) << 7;
+            if (fast) {
+                const int K = 7 - 0x3C00 - e * 128;
+                const uint32_t k16 = (uint32_t)K & 0xFFFFu;
+                const uint32_t k2 = k16 | (((k16 - (K < 0 ? 1u : 0u)) & 0xFFFFu) << 16);
+                const uint32_t c0 = bf16_pair_e4m3(w[0], k2), c1 = bf16_pair_e4m3(w[1], k2);
+                const uint32_t c2 = bf16_pair_e4m3(w[2], k2), c3 = bf16_pair_e4m3(w[3], k2);
+                out.x = __byte_perm(c0, c1, 0x6420);
+                out.y = __byte_perm(c2, c3, 0x6420);
+                sbyte = (uint32_t)(e + 127);
+            } else {
+                uint32_t u[8], c[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    u[2 * i] = w[i] << 16;
+                    u[2 * i + 1] = w[i] & 0xFFFF0000u;
+                }
+                sbyte = quantize8<FMT_E4M3>(u, amax_bits, mn16 << 16, c);
+                out.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+                out.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+            }
+            const bool valid = t < nthreads;
+            const int64_t b = t >> 2;
+            if (valid) __stcs(reinterpret_cast<uint2*>(codes) + t, out);
+            const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 4);
+            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 8);
+            const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 12);
+            const bool words = (nb & 3) == 0;
+            if (valid && (words ? (lane & 15) == 0 : part == 0)) {
+                int64_t off;
+                if (LAYOUT == LAYOUT_ROWMAJOR) {
+                    off = b;
+                } else {
+                    const int64_t r = b / nb, j = b - r * nb;
+                    off = mma_scale_offset(r, j, nb4);
+                }
+                if (words)
+                    *reinterpret_cast<uint32_t*>(scales + off) = sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                else
+                    scales[off] = (uint8_t)sbyte;
+            }
+        }
+        if (kPipe) {
+#pragma unroll
+            for (int q = 0; q < kU; ++q) v[q] = nxt[q % (kPipe ? kU : 1)];
+        } else {
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int64_t t = t0 + (kU + q) * stride;
+                v[q] = t < nthreads ? __ldcs(reinterpret_cast<const uint4*>(x) + t) : make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+    if (LAYOUT == LAYOUT_MMA) write_mma_padding(scales, rows, nb);
 }
 
 template <typename InT, int FMT, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) quantize_kernel(const InT* __restrict__ x, int64_t nblocks, int64_t nb,
                                                             int64_t rows, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ scales) {
-    // 64 bytes of input in flight per thread: 4 items of bf16, 2 of f32
-    constexpr int kU = sizeof(InT) == 2 ? kUnroll : kUnroll / 2;
+    // 64 bytes of input in flight per thread: 4 items of bf16, 2 of f32 (2 when
+    // the tensor-core scale layout's index arithmetic needs the registers)
+    constexpr int kU = (sizeof(InT) == 2 && LAYOUT == LAYOUT_ROWMAJOR) ? kUnroll : kUnroll / 2;
     const int lane = threadIdx.x & 31;
     const int part = lane & 3;  // which 8 of the block's 32 elements
     const int64_t nthreads = nblocks * 4;
@@ -173,13 +332,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) quantize_kernel(const In
         for (int q = 0; q < kU; ++q) {
             const int64_t t = t0 + q * stride;
             if (t - lane >= nthreads) break;  // warp-uniform: whole warp past the end
-            uint32_t m = 0;
+            uint32_t m = 0, mn = 0xFFFFFFFFu;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m = max(m, u[q][i] & 0x7FFFFFFFu);
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t a = u[q][i] & 0x7FFFFFFFu;
+                m = max(m, a);
+                mn = min(mn, a);
+            }
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
             uint32_t c[8];
-            const uint32_t sbyte = quantize8<FMT>(u[q], m, c);
+            const uint32_t sbyte = quantize8<FMT>(u[q], m, mn, c);
             const bool valid = t < nthreads;
             const int64_t b = t >> 2;  // block index
             if (valid) {
@@ -219,27 +382,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) quantize_kernel(const In
         }
     }
 
-    if (LAYOUT == LAYOUT_MMA) {
-        // Padding of the tensor-core layout: rows up to a multiple of 128 and
-        // blocks per row up to a multiple of 4 are written as 0 (scale 2^-127,
-        // finite, so zero-filled operand padding contributes exactly 0).
-        const int64_t r128 = round_up(rows, 128);
-        const int64_t pad_rows = (r128 - rows) * nb4;
-        const int64_t pad_cols = rows * (nb4 - nb);
-        for (int64_t p = (int64_t)blockIdx.x * kThreads + threadIdx.x; p < pad_rows + pad_cols; p += stride) {
-            int64_t r, j;
-            if (p < pad_rows) {
-                r = rows + p / nb4;
-                j = p - (r - rows) * nb4;
-            } else {
-                const int64_t q = p - pad_rows;
-                const int64_t w = nb4 - nb;
-                r = q / w;
-                j = nb + (q - r * w);
-            }
-            scales[mma_scale_offset(r, j, nb4)] = 0;
-        }
-    }
+    if (LAYOUT == LAYOUT_MMA) write_mma_padding(scales, rows, nb);
 }
 
 // --------------------------------------------------------------- dequantize
@@ -260,91 +403,99 @@ __device__ __forceinline__ float e4m3_decode_slow(uint32_t c) {
     return (c & 0x80u) ? -m : m;
 }
 
+// Decode four codes (one E4M3FN word, or the low 16 bits of an E2M1 word)
+// and scale them by `scale` (2^(s-127), or NaN for the poison scale).
+template <int FMT>
+__device__ __forceinline__ float4 decode4(uint32_t w, float scale) {
+    float v[4];
+    if (FMT == FMT_E2M1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t c = (w >> (4 * i)) & 0xFu;
+            const uint32_t m22 = (c & 7u) << 22;
+            const bool sub = m22 < (2u << 22);
+            const uint32_t mag = m22 + (sub ? 0x3F800000u : 0x3F000000u);
+            // exact: the true magnitude is representable and the fma rounds
+            // once; the sign bit goes in afterwards so code 0x8 gives -0.0
+            const float m = __fmaf_rn(__uint_as_float(mag), scale, sub ? -scale : 0.0f);
+            v[i] = __uint_as_float(__float_as_uint(m) | ((c & 8u) << 28));
+        }
+    } else {
+        // fast path unless some code is subnormal (exponent field 0) or NaN
+        if ((__vcmpeq4(w & 0x78787878u, 0u) | __vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu)) == 0u) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t c = (w >> (8 * i)) & 0xFFu;
+                const uint32_t bits = ((c & 0x7Fu) << 20) + 0x3C000000u + ((c & 0x80u) << 24);
+                v[i] = __fmul_rn(__uint_as_float(bits), scale);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(e4m3_decode_slow((w >> (8 * i)) & 0xFFu), scale);
+        }
+    }
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
+
+__device__ __forceinline__ float scale_value(uint32_t s) {
+    // 2^(s-127) as binary32 (s = 0 is the subnormal 2^-127); the NaN scale 0xFF
+    // becomes a NaN multiplier, which poisons the whole block.
+    return s == 0xFFu ? __uint_as_float(0x7FC00000u) : (s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u));
+}
+
+// A warp owns windows of 8 consecutive blocks (256 elements).  Lane t decodes
+// elements [4t, 4t+4) and [128+4t, 128+4t+4) of the window, so each of the
+// warp's two 16-byte store instructions writes 512 contiguous bytes (whole
+// sectors) and each code load reads 128 (E4M3) or 64 (E2M1) contiguous bytes.
 template <int FMT, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const uint8_t* __restrict__ codes,
                                                                           const uint8_t* __restrict__ scales,
                                                                           int64_t nblocks, int64_t nb,
                                                                           float* __restrict__ y) {
-    const int64_t nthreads = nblocks * 4;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwin = (nblocks + 7) / 8;
+    const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
     const int64_t nb4 = round_up(nb, 4);
-    for (int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; t0 < nthreads; t0 += stride * kUnroll) {
-        // issue every load of this round first, then decode and store
-        uint2 w[kUnroll];
-        uint32_t sc[kUnroll];
+    for (int64_t w0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); w0 < nwin; w0 += warps * kUnroll) {
+        uint32_t cw[kUnroll][2];
+        uint32_t sc[kUnroll][2];
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
-            const int64_t t = t0 + q * stride;
-            w[q] = make_uint2(0, 0);
-            sc[q] = 0;
-            if (t < nthreads) {
-                const int64_t b = t >> 2;
-                int64_t soff;
-                if (LAYOUT == LAYOUT_ROWMAJOR) {
-                    soff = b;
-                } else {
-                    const int64_t r = b / nb, j = b - r * nb;
-                    soff = mma_scale_offset(r, j, nb4);
+            const int64_t win = w0 + q * warps;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t b = win * 8 + 4 * h + (lane >> 3);  // block of this half
+                cw[q][h] = 0;
+                sc[q][h] = 0;
+                if (win < nwin && b < nblocks) {
+                    int64_t soff;
+                    if (LAYOUT == LAYOUT_ROWMAJOR) {
+                        soff = b;
+                    } else {
+                        const int64_t r = b / nb, j = b - r * nb;
+                        soff = mma_scale_offset(r, j, nb4);
+                    }
+                    sc[q][h] = __ldg(scales + soff);
+                    const int64_t e = win * 256 + 128 * h + 4 * lane;  // first element
+                    if (FMT == FMT_E2M1)
+                        cw[q][h] = __ldcs(reinterpret_cast<const uint16_t*>(codes) + e / 4);
+                    else
+                        cw[q][h] = __ldcs(reinterpret_cast<const uint32_t*>(codes) + e / 4);
                 }
-                sc[q] = __ldg(scales + soff);
-                if (FMT == FMT_E2M1)
-                    w[q].x = __ldcs(reinterpret_cast<const uint32_t*>(codes) + t);
-                else
-                    w[q] = __ldcs(reinterpret_cast<const uint2*>(codes) + t);
             }
         }
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
-            const int64_t t = t0 + q * stride;
-            if (t >= nthreads) break;
-            const uint32_t s = sc[q];
-            uint32_t c[8];
-            if (FMT == FMT_E2M1) {
+            const int64_t win = w0 + q * warps;
+            if (win >= nwin) break;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) c[i] = (w[q].x >> (4 * i)) & 0xFu;
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    c[i] = (w[q].x >> (8 * i)) & 0xFFu;
-                    c[4 + i] = (w[q].y >> (8 * i)) & 0xFFu;
+            for (int h = 0; h < 2; ++h) {
+                const int64_t b = win * 8 + 4 * h + (lane >> 3);
+                if (b < nblocks) {
+                    const int64_t e = win * 256 + 128 * h + 4 * lane;
+                    __stcs(reinterpret_cast<float4*>(y + e), decode4<FMT>(cw[q][h], scale_value(sc[q][h])));
                 }
             }
-            // 2^(s-127) as binary32 (s = 0 is the subnormal 2^-127); the NaN scale
-            // 0xFF becomes a NaN multiplier, which poisons the whole block.
-            const float scale = s == 0xFFu ? __uint_as_float(0x7FC00000u)
-                                           : (s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u));
-            float v[8];
-            if (FMT == FMT_E2M1) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t m22 = (c[i] & 7u) << 22;
-                    const bool sub = m22 < (2u << 22);
-                    const uint32_t mag = m22 + (sub ? 0x3F800000u : 0x3F000000u);
-                    // exact: the true magnitude is representable and the fma rounds
-                    // once; the sign bit goes in afterwards so code 0x8 gives -0.0
-                    const float m = __fmaf_rn(__uint_as_float(mag), scale, sub ? -scale : 0.0f);
-                    v[i] = __uint_as_float(__float_as_uint(m) | ((c[i] & 8u) << 28));
-                }
-            } else {
-                // fast path unless some code is subnormal (exponent field 0) or NaN
-                const uint32_t w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-                const uint32_t w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-                const uint32_t slow = __vcmpeq4(w0 & 0x78787878u, 0u) | __vcmpeq4(w0 & 0x7F7F7F7Fu, 0x7F7F7F7Fu) |
-                                      __vcmpeq4(w1 & 0x78787878u, 0u) | __vcmpeq4(w1 & 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-                if (slow == 0u) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t bits = ((c[i] & 0x7Fu) << 20) + 0x3C000000u + ((c[i] & 0x80u) << 24);
-                        v[i] = __fmul_rn(__uint_as_float(bits), scale);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(e4m3_decode_slow(c[i]), scale);
-                }
-            }
-            float4* out = reinterpret_cast<float4*>(y) + t * 2;
-            __stcs(out, make_float4(v[0], v[1], v[2], v[3]));
-            __stcs(out + 1, make_float4(v[4], v[5], v[6], v[7]));
         }
     }
 }
@@ -385,8 +536,22 @@ template <typename InT, int FMT>
 cudaError_t quant_dispatch_layout(const InT* x, int64_t nblocks, int64_t nb, int64_t rows, uint8_t* codes,
                                   uint8_t* scales, int layout, cudaStream_t st) {
     const int64_t work = nblocks * 4;
-    constexpr int kU = sizeof(InT) == 2 ? kUnroll : kUnroll / 2;
-    int64_t grid = grid_for((work + kU - 1) / kU, kMinBlocks);
+    int64_t grid = grid_for((work + 1) / 2, kMinBlocks);
+    if constexpr (sizeof(InT) == 2 && FMT == FMT_E4M3) {
+        if (layout == LAYOUT_MMA) {
+            const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
+            const int64_t g2 = grid_for(pad, kMinBlocks);
+            grid = grid > g2 ? grid : g2;
+            quantize_bf16_e4m3_kernel<LAYOUT_MMA, 2, kMinBlocks, 1><<<(unsigned)grid, kThreads, 0, st>>>(x, nblocks, nb, rows, codes, scales);
+        } else {
+            // two items per thread per round, the next round's loads issued before
+            // this round's work (measured fastest of the unroll / occupancy choices)
+            const unsigned g = (unsigned)grid_for((work + 1) / 2, kMinBlocks);
+            quantize_bf16_e4m3_kernel<LAYOUT_ROWMAJOR, 2, kMinBlocks, 1><<<g, kThreads, 0, st>>>(x, nblocks, nb, rows,
+                                                                                                codes, scales);
+        }
+        return cudaGetLastError();
+    }
     if (layout == LAYOUT_MMA) {
         const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
         const int64_t g2 = grid_for(pad, 8);
@@ -421,7 +586,9 @@ cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t 
                               int layout, float* y, cudaStream_t st) {
     const int64_t nb = cols / 32;
     const int64_t nblocks = rows * nb;
-    const unsigned grid = (unsigned)grid_for((nblocks * 4 + kUnroll - 1) / kUnroll, kMinBlocks);
+    // one warp per window of 8 blocks, kUnroll windows per warp per round
+    const int64_t nwin = (nblocks + 7) / 8;
+    const unsigned grid = (unsigned)grid_for((nwin * 32 + kUnroll - 1) / kUnroll, kMinBlocks);
     const uint8_t* c = static_cast<const uint8_t*>(codes);
     if (fmt == FMT_E2M1) {
         if (layout == LAYOUT_MMA)
