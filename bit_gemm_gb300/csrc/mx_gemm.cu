@@ -75,7 +75,6 @@ struct GemmParams {
     int32_t swap;          // 1: C(q, p) += acc(p, q)  (operands swapped)
     int32_t use_tma_epi;   // 1: C map valid (TMA reduce-add epilogue), 0: per-element atomics
     int32_t epi_red_v4;    // 1: write C with vector reductions instead of TMA (BN = 256 path)
-    int32_t k_rotate;      // 1: rotate each tile's K loop by its M-tile index
     float* C;
     int64_t ldc;
     const uint8_t* sfa;    // scales of the MMA A operand (tensor-core layout)
@@ -87,7 +86,6 @@ struct GemmParams {
 
 struct Work {
     int32_t tp, tq, kb0, kb1;
-    int32_t rot;  // the K loop starts `rot` stages into [kb0, kb1) and wraps
 };
 
 // The iter-th unit of work of this CTA; identical in every role.
@@ -112,11 +110,6 @@ __device__ __forceinline__ bool get_work(const GemmParams& p, int iter, Work& w)
     }
     w.tp = (int32_t)(tile % p.tiles_p);
     w.tq = (int32_t)(tile / p.tiles_p);
-    // Concurrently running tiles share a B tile and differ in their M tile;
-    // starting each M tile at a different K stage keeps them from requesting
-    // the same lines of B at the same moment.  Only the order of the f32
-    // partial sums changes.
-    w.rot = (p.mode == 0 && p.k_rotate) ? (int32_t)(((int64_t)w.tp * (w.kb1 - w.kb0)) / p.tiles_p) : 0;
     return true;
 }
 
@@ -229,9 +222,11 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
             const int32_t q0 = w.tq * BN;
             const int nk = w.kb1 - w.kb0;
             for (int j = 0; j < nk; ++j) {
-                const int kb = w.kb0 + (j + w.rot) % nk;
+                const int kb = w.kb0 + j;
+                // (the abort flag is consulted only when a bounded wait gives up:
+                // a shared-memory load and branch per stage would delay issue)
                 int okw = 1;
-                if (lane == 0) okw = !*abort_flag && mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
+                if (lane == 0) okw = mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
                 okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
                 if (!okw) {
                     if (lane == 0) *abort_flag = 1;
@@ -333,8 +328,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                 const uint32_t d_tmem = tmem + kAccCol + acc * BN;
                 const int nk = w.kb1 - w.kb0;
                 for (int j = 0; j < nk; ++j) {
-                    const int kb = w.kb0 + (j + w.rot) % nk;
-                    if (*abort_flag || !mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
+                    const int kb = w.kb0 + j;
+                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -749,7 +744,6 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     p.swap = swap ? 1 : 0;
     p.use_tma_epi = tma_epi ? 1 : 0;
     p.epi_red_v4 = 0;  // TMA reduce-add measured faster than vector reductions on GB300
-    p.k_rotate = 0;    // K-loop rotation measured no gain
     p.C = a.C;
     p.ldc = a.N;
     p.sfa = x_sf;
