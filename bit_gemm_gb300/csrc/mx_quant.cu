@@ -8,11 +8,16 @@
 //
 // Both kernels stream HBM.  A tensor of R x C (C % 32 == 0) is, in memory, a
 // run of R*C/32 blocks of 32 contiguous elements, so the kernels index blocks
-// directly: four threads own one block (8 elements each, one or two 16-byte
-// loads), a warp owns 8 consecutive blocks (1 KB of f32 / 512 B of bf16, fully
-// coalesced), and the block maximum is two xor-shuffles.  Rounding is integer
-// and compare logic on the binary32 bits -- no math library calls -- and the
-// file is built without flush-to-zero so subnormal inputs and outputs are exact.
+// directly.  bf16 input (32-byte aligned): one thread owns one block (two
+// 256-bit loads, one 256- or 128-bit store of codes), so the per-block work --
+// amax, scale, its store -- is done once, and elements are rounded by the
+// hardware E4M3 / E2M1 conversions after an exact pre-scaling that turns
+// their ties-to-even into ties-to-lower.  f32 input (and bf16 that is only
+// 16-byte aligned): four threads own one block (8 elements each), a warp owns
+// 8 consecutive blocks (fully coalesced), the block maximum is two
+// xor-shuffles, and rounding is integer and compare logic on the binary32
+// bits.  No math library calls; the file is built without flush-to-zero so
+// subnormal inputs and outputs are exact.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -185,117 +190,150 @@ __device__ __forceinline__ uint32_t quantize8(const uint32_t (&u)[8], uint32_t a
     return (uint32_t)(e + 127);
 }
 
-// bf16 -> E4M3FN, two elements per 32-bit word (the low half is the lower
-// element).  For a block whose exponent e >= -120 and whose elements all lie
-// at or above the E4M3 normal range (|x| >= 2^(e-6)), each half h of a word
-// gives its code as ((h - (e << 7)) + 7 - (120 << 7)) >> 4: subtract e from
-// the bf16 exponent field, round the 4 dropped mantissa bits half-down,
-// re-bias 127 -> 7.  Both halves are formed by one 32-bit add: the low half's
-// carry into the high half is 1 exactly when the constant K is negative, so
-// it is pre-subtracted from the high half of the constant.
-__device__ __forceinline__ uint32_t bf16_pair_e4m3(uint32_t w, uint32_t k2) {
-    const uint32_t t = (w & 0x7FFF7FFFu) + k2;                      // r_lo | r_hi << 16
-    uint32_t c = __vminu2((t >> 4) & 0x00FF00FFu, 0x007E007Eu);      // saturate at 448
-    return c | ((w >> 8) & 0x00800080u);                            // sign bits 15, 31 -> 7, 23
+// ------------------------------------------------- bf16: one thread per block
+//
+// A bf16 element has 8 significant bits, so y = x * 2^-e * (1 - 2^-12) is
+// exact in binary32 (8 + 12 bits).  It sits below x * 2^-e by less than 2^-11
+// of its magnitude, which is less than the distance (at least one bf16 unit in
+// the last place) from any value that is not a tie to the nearest rounding
+// midpoint of either element grid; a tie moves strictly below its midpoint.
+// The hardware conversion (round to nearest even, saturating at the largest
+// finite code) therefore rounds every tie to the LOWER magnitude and every
+// other value as exact rounding would: the first-index argmin rule of
+// "Reference encode and decode".  The multiply is a fused multiply-add with
+// +0 so that -0.0 becomes +0 (the sign bit is set only for x < 0), while a
+// nonzero negative x keeps its sign even when it rounds to zero.  Saturation
+// covers |x| 2^-e in (max, 2^(emax+1)), where the nearest grid point is the
+// format's largest.
+
+// 64 bytes of bf16 (one block) in two 256-bit loads; p is 32-byte aligned.
+__device__ __forceinline__ void load_block_bf16(const __nv_bfloat16* p, uint32_t (&w)[16]) {
+    asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15])
+        : "l"(p + 16));
 }
 
-template <int LAYOUT, int kU, int kMB, int kPipe>
-__global__ void __launch_bounds__(kThreads, kMB)
-    quantize_bf16_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int64_t nblocks, int64_t nb, int64_t rows,
-                              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-    const int lane = threadIdx.x & 31;
-    const int part = lane & 3;
-    const int64_t nthreads = nblocks * 4;
+// four binary32 -> four E4M3FN codes, element 0 in byte 0
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    return r;
+}
+
+// eight binary32 -> eight E2M1 codes, element 0 in the low nibble of byte 0
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&a)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(a[0]), "f"(a[1]), "f"(a[2]), "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7]));
+    return r;
+}
+
+// Quantize one block of 32 bf16 (16 words, low half = lower element).
+// Returns the scale byte; fills 32 bytes (E4M3FN) or 16 bytes (E2M1) of codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_block_bf16(const uint32_t (&w)[16], uint32_t (&out)[FMT == FMT_E2M1 ? 4 : 8]) {
+    constexpr int kEmax = FMT == FMT_E2M1 ? 2 : 8;
+    uint32_t m2 = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+    for (int i = 1; i < 16; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);  // bf16 bits of the block's amax
+    if (m >= 0x7F80u) {  // NaN or infinity in the block: poison it
+#pragma unroll
+        for (int i = 0; i < (FMT == FMT_E2M1 ? 4 : 8); ++i) out[i] = 0;
+        return 0xFFu;
+    }
+    // floor(log2 amax) from the bits: normal 2^(field-127), subnormal m * 2^-133
+    const int fe = (int)(m >> 7);
+    const int E = fe ? fe - 127 : (31 - __clz((int)m)) - 133;
+    int e = E - kEmax;
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    e = m ? e : 0;  // all-zero block: scale byte 127, codes +0
+    // 2^-e * (1 - 2^-12) = 2^(-e-1) * (2 - 2^-11)
+    const float c = __uint_as_float(((uint32_t)(126 - e) << 23) | 0x7FF000u);
+    float y[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        y[2 * i] = __fmaf_rn(__uint_as_float(w[i] << 16), c, 0.0f);
+        y[2 * i + 1] = __fmaf_rn(__uint_as_float(w[i] & 0xFFFF0000u), c, 0.0f);
+    }
+    if (FMT == FMT_E2M1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float a[8] = {y[8 * k], y[8 * k + 1], y[8 * k + 2], y[8 * k + 3],
+                                y[8 * k + 4], y[8 * k + 5], y[8 * k + 6], y[8 * k + 7]};
+            out[k] = cvt_e2m1x8(a);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) out[k] = cvt_e4m3x4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+    }
+    return (uint32_t)(e + 127);
+}
+
+// Grid-strided over blocks, kU blocks per thread in flight.  x and codes are
+// 32-byte aligned.  For the tensor-core scale layout the block's (row, block
+// column) is carried incrementally across the stride.
+template <int FMT, int LAYOUT, int kU>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    quantize_bf16_block_kernel(const __nv_bfloat16* __restrict__ x, int64_t nblocks, int64_t nb, int64_t rows,
+                               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    constexpr int kCodeWords = FMT == FMT_E2M1 ? 4 : 8;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const int64_t nb4 = round_up(nb, 4);
-    uint4 v[kU], nxt[kPipe ? kU : 1];
-    int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-#pragma unroll
-    for (int q = 0; q < kU; ++q) {
-        const int64_t t = t0 + q * stride;
-        v[q] = t < nthreads ? __ldcs(reinterpret_cast<const uint4*>(x) + t) : make_uint4(0, 0, 0, 0);
+    int64_t b0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    // (row, column) of block b0 and of the stride, for the tensor-core layout
+    int32_t r = 0, j = 0, sr = 0, sj = 0;  // rows, blocks per row and the stride are below 2^31
+    if (LAYOUT == LAYOUT_MMA) {
+        r = (int32_t)(b0 / nb);
+        j = (int32_t)(b0 - (int64_t)r * nb);
+        sr = (int32_t)(stride / nb);
+        sj = (int32_t)(stride - (int64_t)sr * nb);
     }
-    for (; t0 - lane < nthreads; t0 += stride * kU) {
-        if (kPipe) {
-            // issue the next round's loads before working on this round
+    for (; b0 < nblocks; b0 += stride * kU) {
+        uint32_t w[kU][16];
 #pragma unroll
-            for (int q = 0; q < kU; ++q) {
-                const int64_t t = t0 + (kU + q) * stride;
-                nxt[q % (kPipe ? kU : 1)] = t < nthreads ? __ldcs(reinterpret_cast<const uint4*>(x) + t) : make_uint4(0, 0, 0, 0);
-            }
+        for (int q = 0; q < kU; ++q) {
+            const int64_t b = b0 + q * stride;
+            if (b < nblocks) load_block_bf16(x + 32 * b, w[q]);
         }
 #pragma unroll
         for (int q = 0; q < kU; ++q) {
-            const int64_t t = t0 + q * stride;
-            if (t - lane >= nthreads) break;  // warp-uniform
-            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-            // |bits| max and min over the thread's 8 elements, 16 bits per lane
-            uint32_t mx2 = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                    __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
-            uint32_t mn2 = __vminu2(__vminu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                    __vminu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
-            uint32_t m = max(mx2 & 0xFFFFu, mx2 >> 16);
-            const uint32_t mn16 = min(mn2 & 0xFFFFu, mn2 >> 16);
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            const uint32_t amax_bits = m << 16;  // binary32 pattern of the bf16 amax
-            uint32_t sbyte;
-            uint2 out;
-            // fast path conditions (a finite, nonzero block is required)
-            const int fe = (int)(amax_bits >> 23);
-            int e = (fe ? fe - 127 : (31 - __clz((int)amax_bits)) - 149) - 8;
-            e = e < -127 ? -127 : (e > 127 ? 127 : e);
-            const bool fast = amax_bits - 1u < 0x7F7FFFFFu  // nonzero and finite
-                              && e >= -120 && mn16 >= (uint32_t)(e + 121) << 7;
-            if (fast) {
-                const int K = 7 - 0x3C00 - e * 128;
-                const uint32_t k16 = (uint32_t)K & 0xFFFFu;
-                const uint32_t k2 = k16 | (((k16 - (K < 0 ? 1u : 0u)) & 0xFFFFu) << 16);
-                const uint32_t c0 = bf16_pair_e4m3(w[0], k2), c1 = bf16_pair_e4m3(w[1], k2);
-                const uint32_t c2 = bf16_pair_e4m3(w[2], k2), c3 = bf16_pair_e4m3(w[3], k2);
-                out.x = __byte_perm(c0, c1, 0x6420);
-                out.y = __byte_perm(c2, c3, 0x6420);
-                sbyte = (uint32_t)(e + 127);
+            const int64_t b = b0 + q * stride;
+            if (b >= nblocks) break;
+            uint32_t out[kCodeWords];
+            const uint32_t sbyte = quantize_block_bf16<FMT>(w[q], out);
+            if (FMT == FMT_E2M1) {
+                __stcs(reinterpret_cast<uint4*>(codes) + b, make_uint4(out[0], out[1], out[2], out[3]));
             } else {
-                uint32_t u[8], c[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    u[2 * i] = w[i] << 16;
-                    u[2 * i + 1] = w[i] & 0xFFFF0000u;
-                }
-                sbyte = quantize8<FMT_E4M3>(u, amax_bits, mn16 << 16, c);
-                out.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-                out.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+                asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(codes + 32 * b),
+                             "r"(out[0]), "r"(out[1]), "r"(out[2]), "r"(out[3]), "r"(out[4]), "r"(out[5]),
+                             "r"(out[6]), "r"(out[7])
+                             : "memory");
             }
-            const bool valid = t < nthreads;
-            const int64_t b = t >> 2;
-            if (valid) __stcs(reinterpret_cast<uint2*>(codes) + t, out);
-            const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 4);
-            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 8);
-            const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 12);
-            const bool words = (nb & 3) == 0;
-            if (valid && (words ? (lane & 15) == 0 : part == 0)) {
-                int64_t off;
-                if (LAYOUT == LAYOUT_ROWMAJOR) {
-                    off = b;
-                } else {
-                    const int64_t r = b / nb, j = b - r * nb;
-                    off = mma_scale_offset(r, j, nb4);
+            if (LAYOUT == LAYOUT_MMA) {
+                scales[mma_scale_offset(r, j, nb4)] = (uint8_t)sbyte;
+                r += sr;
+                j += sj;
+                if (j >= nb) {
+                    j -= nb;
+                    ++r;
                 }
-                if (words)
-                    *reinterpret_cast<uint32_t*>(scales + off) = sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
-                else
-                    scales[off] = (uint8_t)sbyte;
-            }
-        }
-        if (kPipe) {
-#pragma unroll
-            for (int q = 0; q < kU; ++q) v[q] = nxt[q % (kPipe ? kU : 1)];
-        } else {
-#pragma unroll
-            for (int q = 0; q < kU; ++q) {
-                const int64_t t = t0 + (kU + q) * stride;
-                v[q] = t < nthreads ? __ldcs(reinterpret_cast<const uint4*>(x) + t) : make_uint4(0, 0, 0, 0);
+            } else {
+                scales[b] = (uint8_t)sbyte;
             }
         }
     }
@@ -387,54 +425,43 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) quantize_kernel(const In
 
 // --------------------------------------------------------------- dequantize
 
-// Decoding assembles binary32 bits directly.
-//  E4M3FN normal (exponent field E >= 1): 2^(E-7) (1 + M/8) has the bits
-//    (E + 120) << 23 | M << 20 = (code7 << 20) + (120 << 23).
-//  E4M3FN subnormal (E = 0): M * 2^-9, exact in binary32.  Code 0x7F is NaN.
-//  E2M1 (E >= 1): 2^(E-1) (1 + M/2) has the bits (code3 << 22) + (126 << 23);
-//    for E = 0 the same assembly with exponent 127 gives 1 + M/2, and 1.0 is
-//    subtracted afterwards (0 and 0.5).
-__device__ __forceinline__ float e4m3_decode_slow(uint32_t c) {
-    const uint32_t c7 = c & 0x7Fu;
-    float m;
-    if (c7 == 0x7Fu) m = __uint_as_float(0x7FC00000u);
-    else if (c7 < 8u) m = (float)c7 * 0.001953125f;
-    else m = __uint_as_float((c7 << 20) + 0x3C000000u);
-    return (c & 0x80u) ? -m : m;
+// Decoding uses the hardware conversions E4M3FN / E2M1 -> f16 (exact: every
+// element value, and the E4M3FN NaN code, is representable in f16), then
+// f16 -> f32 (exact) and one multiply by the block's scale 2^(s-127), which
+// is exact too: the smallest product, 2^-9 * 2^-127, is a binary32
+// subnormal, and a product above the binary32 range is infinite, as the
+// exact value rounded to binary32 is.  A NaN scale makes every product NaN.
+
+// eight E4M3FN codes (byte i = element i) -> eight f32, times `mult`
+__device__ __forceinline__ void decode8_e4m3(uint32_t lo, uint32_t hi, float mult, float (&v)[8]) {
+    asm("{\n\t.reg .b16 c0, c1, c2, c3, h0, h1, h2, h3, h4, h5, h6, h7;\n\t"
+        ".reg .b32 p0, p1, p2, p3;\n\t.reg .f32 f0, f1, f2, f3, f4, f5, f6, f7;\n\t"
+        "mov.b32 {c0, c1}, %8;\n\tmov.b32 {c2, c3}, %9;\n\t"
+        "cvt.rn.f16x2.e4m3x2 p0, c0;\n\tcvt.rn.f16x2.e4m3x2 p1, c1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 p2, c2;\n\tcvt.rn.f16x2.e4m3x2 p3, c3;\n\t"
+        "mov.b32 {h0, h1}, p0;\n\tmov.b32 {h2, h3}, p1;\n\tmov.b32 {h4, h5}, p2;\n\tmov.b32 {h6, h7}, p3;\n\t"
+        "cvt.f32.f16 f0, h0;\n\tcvt.f32.f16 f1, h1;\n\tcvt.f32.f16 f2, h2;\n\tcvt.f32.f16 f3, h3;\n\t"
+        "cvt.f32.f16 f4, h4;\n\tcvt.f32.f16 f5, h5;\n\tcvt.f32.f16 f6, h6;\n\tcvt.f32.f16 f7, h7;\n\t"
+        "mul.rn.f32 %0, f0, %10;\n\tmul.rn.f32 %1, f1, %10;\n\tmul.rn.f32 %2, f2, %10;\n\tmul.rn.f32 %3, f3, %10;\n\t"
+        "mul.rn.f32 %4, f4, %10;\n\tmul.rn.f32 %5, f5, %10;\n\tmul.rn.f32 %6, f6, %10;\n\tmul.rn.f32 %7, f7, %10;\n\t}"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+        : "r"(lo), "r"(hi), "f"(mult));
 }
 
-// Decode four codes (one E4M3FN word, or the low 16 bits of an E2M1 word)
-// and scale them by `scale` (2^(s-127), or NaN for the poison scale).
-template <int FMT>
-__device__ __forceinline__ float4 decode4(uint32_t w, float scale) {
-    float v[4];
-    if (FMT == FMT_E2M1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t c = (w >> (4 * i)) & 0xFu;
-            const uint32_t m22 = (c & 7u) << 22;
-            const bool sub = m22 < (2u << 22);
-            const uint32_t mag = m22 + (sub ? 0x3F800000u : 0x3F000000u);
-            // exact: the true magnitude is representable and the fma rounds
-            // once; the sign bit goes in afterwards so code 0x8 gives -0.0
-            const float m = __fmaf_rn(__uint_as_float(mag), scale, sub ? -scale : 0.0f);
-            v[i] = __uint_as_float(__float_as_uint(m) | ((c & 8u) << 28));
-        }
-    } else {
-        // fast path unless some code is subnormal (exponent field 0) or NaN
-        if ((__vcmpeq4(w & 0x78787878u, 0u) | __vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu)) == 0u) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t c = (w >> (8 * i)) & 0xFFu;
-                const uint32_t bits = ((c & 0x7Fu) << 20) + 0x3C000000u + ((c & 0x80u) << 24);
-                v[i] = __fmul_rn(__uint_as_float(bits), scale);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(e4m3_decode_slow((w >> (8 * i)) & 0xFFu), scale);
-        }
-    }
-    return make_float4(v[0], v[1], v[2], v[3]);
+// eight E2M1 codes (element i in nibble i, low nibble first) -> eight f32, times `mult`
+__device__ __forceinline__ void decode8_e2m1(uint32_t w, float mult, float (&v)[8]) {
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t.reg .b16 h0, h1, h2, h3, h4, h5, h6, h7;\n\t"
+        ".reg .b32 p0, p1, p2, p3;\n\t.reg .f32 f0, f1, f2, f3, f4, f5, f6, f7;\n\t"
+        "mov.b32 {c0, c1, c2, c3}, %8;\n\t"
+        "cvt.rn.f16x2.e2m1x2 p0, c0;\n\tcvt.rn.f16x2.e2m1x2 p1, c1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 p2, c2;\n\tcvt.rn.f16x2.e2m1x2 p3, c3;\n\t"
+        "mov.b32 {h0, h1}, p0;\n\tmov.b32 {h2, h3}, p1;\n\tmov.b32 {h4, h5}, p2;\n\tmov.b32 {h6, h7}, p3;\n\t"
+        "cvt.f32.f16 f0, h0;\n\tcvt.f32.f16 f1, h1;\n\tcvt.f32.f16 f2, h2;\n\tcvt.f32.f16 f3, h3;\n\t"
+        "cvt.f32.f16 f4, h4;\n\tcvt.f32.f16 f5, h5;\n\tcvt.f32.f16 f6, h6;\n\tcvt.f32.f16 f7, h7;\n\t"
+        "mul.rn.f32 %0, f0, %9;\n\tmul.rn.f32 %1, f1, %9;\n\tmul.rn.f32 %2, f2, %9;\n\tmul.rn.f32 %3, f3, %9;\n\t"
+        "mul.rn.f32 %4, f4, %9;\n\tmul.rn.f32 %5, f5, %9;\n\tmul.rn.f32 %6, f6, %9;\n\tmul.rn.f32 %7, f7, %9;\n\t}"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+        : "r"(w), "f"(mult));
 }
 
 __device__ __forceinline__ float scale_value(uint32_t s) {
@@ -444,10 +471,11 @@ __device__ __forceinline__ float scale_value(uint32_t s) {
 }
 
 // A warp owns windows of 8 consecutive blocks (256 elements).  Lane t decodes
-// elements [4t, 4t+4) and [128+4t, 128+4t+4) of the window, so each of the
-// warp's two 16-byte store instructions writes 512 contiguous bytes (whole
-// sectors) and each code load reads 128 (E4M3) or 64 (E2M1) contiguous bytes.
-template <int FMT, int LAYOUT>
+// elements [8t, 8t+8) of the window (block t/4), so one warp store writes 1 KB
+// of contiguous f32 (one 256-bit store per lane when y is 32-byte aligned,
+// else two 128-bit stores) and one code load reads 256 (E4M3) or 128 (E2M1)
+// contiguous bytes.
+template <int FMT, int LAYOUT, bool kV8>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const uint8_t* __restrict__ codes,
                                                                           const uint8_t* __restrict__ scales,
                                                                           int64_t nblocks, int64_t nb,
@@ -458,29 +486,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const 
     const int64_t nb4 = round_up(nb, 4);
     for (int64_t w0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); w0 < nwin; w0 += warps * kUnroll) {
         uint32_t cw[kUnroll][2];
-        uint32_t sc[kUnroll][2];
+        uint32_t sc[kUnroll];
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
             const int64_t win = w0 + q * warps;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int64_t b = win * 8 + 4 * h + (lane >> 3);  // block of this half
-                cw[q][h] = 0;
-                sc[q][h] = 0;
-                if (win < nwin && b < nblocks) {
-                    int64_t soff;
-                    if (LAYOUT == LAYOUT_ROWMAJOR) {
-                        soff = b;
-                    } else {
-                        const int64_t r = b / nb, j = b - r * nb;
-                        soff = mma_scale_offset(r, j, nb4);
-                    }
-                    sc[q][h] = __ldg(scales + soff);
-                    const int64_t e = win * 256 + 128 * h + 4 * lane;  // first element
-                    if (FMT == FMT_E2M1)
-                        cw[q][h] = __ldcs(reinterpret_cast<const uint16_t*>(codes) + e / 4);
-                    else
-                        cw[q][h] = __ldcs(reinterpret_cast<const uint32_t*>(codes) + e / 4);
+            const int64_t b = win * 8 + (lane >> 2);  // this lane's block
+            cw[q][0] = cw[q][1] = sc[q] = 0;
+            if (win < nwin && b < nblocks) {
+                int64_t soff;
+                if (LAYOUT == LAYOUT_ROWMAJOR) {
+                    soff = b;
+                } else {
+                    const int64_t r = b / nb, j = b - r * nb;
+                    soff = mma_scale_offset(r, j, nb4);
+                }
+                sc[q] = __ldg(scales + soff);
+                const int64_t e = win * 256 + 8 * lane;  // first element
+                if (FMT == FMT_E2M1) {
+                    cw[q][0] = __ldcs(reinterpret_cast<const uint32_t*>(codes) + e / 8);
+                } else {
+                    const uint2 c2 = __ldcs(reinterpret_cast<const uint2*>(codes) + e / 8);
+                    cw[q][0] = c2.x;
+                    cw[q][1] = c2.y;
                 }
             }
         }
@@ -488,12 +515,20 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const 
         for (int q = 0; q < kUnroll; ++q) {
             const int64_t win = w0 + q * warps;
             if (win >= nwin) break;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int64_t b = win * 8 + 4 * h + (lane >> 3);
-                if (b < nblocks) {
-                    const int64_t e = win * 256 + 128 * h + 4 * lane;
-                    __stcs(reinterpret_cast<float4*>(y + e), decode4<FMT>(cw[q][h], scale_value(sc[q][h])));
+            const int64_t b = win * 8 + (lane >> 2);
+            if (b < nblocks) {
+                float v[8];
+                const float mult = scale_value(sc[q]);
+                if (FMT == FMT_E2M1) decode8_e2m1(cw[q][0], mult, v);
+                else decode8_e4m3(cw[q][0], cw[q][1], mult, v);
+                float* dst = y + win * 256 + 8 * lane;
+                if (kV8) {
+                    asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "f"(v[0]),
+                                 "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                                 : "memory");
+                } else {
+                    __stcs(reinterpret_cast<float4*>(dst), make_float4(v[0], v[1], v[2], v[3]));
+                    __stcs(reinterpret_cast<float4*>(dst) + 1, make_float4(v[4], v[5], v[6], v[7]));
                 }
             }
         }
@@ -537,20 +572,23 @@ cudaError_t quant_dispatch_layout(const InT* x, int64_t nblocks, int64_t nb, int
                                   uint8_t* scales, int layout, cudaStream_t st) {
     const int64_t work = nblocks * 4;
     int64_t grid = grid_for((work + 1) / 2, kMinBlocks);
-    if constexpr (sizeof(InT) == 2 && FMT == FMT_E4M3) {
-        if (layout == LAYOUT_MMA) {
-            const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
-            const int64_t g2 = grid_for(pad, kMinBlocks);
-            grid = grid > g2 ? grid : g2;
-            quantize_bf16_e4m3_kernel<LAYOUT_MMA, 2, kMinBlocks, 1><<<(unsigned)grid, kThreads, 0, st>>>(x, nblocks, nb, rows, codes, scales);
-        } else {
-            // two items per thread per round, the next round's loads issued before
-            // this round's work (measured fastest of the unroll / occupancy choices)
-            const unsigned g = (unsigned)grid_for((work + 1) / 2, kMinBlocks);
-            quantize_bf16_e4m3_kernel<LAYOUT_ROWMAJOR, 2, kMinBlocks, 1><<<g, kThreads, 0, st>>>(x, nblocks, nb, rows,
+    const bool al32 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(codes)) & 31) == 0;
+    if constexpr (sizeof(InT) == 2) {
+        if (al32) {
+            constexpr int kU = 2;
+            int64_t g = grid_for((nblocks + kU - 1) / kU, kMinBlocks);
+            if (layout == LAYOUT_MMA) {
+                const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
+                const int64_t g2 = grid_for(pad, kMinBlocks);
+                g = g > g2 ? g : g2;
+                quantize_bf16_block_kernel<FMT, LAYOUT_MMA, kU><<<(unsigned)g, kThreads, 0, st>>>(x, nblocks, nb, rows,
                                                                                                 codes, scales);
+            } else {
+                quantize_bf16_block_kernel<FMT, LAYOUT_ROWMAJOR, kU><<<(unsigned)g, kThreads, 0, st>>>(
+                    x, nblocks, nb, rows, codes, scales);
+            }
+            return cudaGetLastError();
         }
-        return cudaGetLastError();
     }
     if (layout == LAYOUT_MMA) {
         const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
@@ -560,6 +598,23 @@ cudaError_t quant_dispatch_layout(const InT* x, int64_t nblocks, int64_t nb, int
     } else {
         quantize_kernel<InT, FMT, LAYOUT_ROWMAJOR><<<(unsigned)grid, kThreads, 0, st>>>(x, nblocks, nb, rows, codes,
                                                                                       scales);
+    }
+    return cudaGetLastError();
+}
+
+template <bool kV8>
+cudaError_t deq_dispatch(const uint8_t* c, const uint8_t* scales, int64_t nblocks, int64_t nb, int fmt, int layout,
+                         float* y, unsigned grid, cudaStream_t st) {
+    if (fmt == FMT_E2M1) {
+        if (layout == LAYOUT_MMA)
+            dequantize_kernel<FMT_E2M1, LAYOUT_MMA, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+        else
+            dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+    } else {
+        if (layout == LAYOUT_MMA)
+            dequantize_kernel<FMT_E4M3, LAYOUT_MMA, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+        else
+            dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
     }
     return cudaGetLastError();
 }
@@ -590,19 +645,11 @@ cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t 
     const int64_t nwin = (nblocks + 7) / 8;
     const unsigned grid = (unsigned)grid_for((nwin * 32 + kUnroll - 1) / kUnroll, kMinBlocks);
     const uint8_t* c = static_cast<const uint8_t*>(codes);
-    if (fmt == FMT_E2M1) {
-        if (layout == LAYOUT_MMA)
-            dequantize_kernel<FMT_E2M1, LAYOUT_MMA><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
-        else
-            dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
-    } else {
-        if (layout == LAYOUT_MMA)
-            dequantize_kernel<FMT_E4M3, LAYOUT_MMA><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
-        else
-            dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
-    }
-    return cudaGetLastError();
+    if ((reinterpret_cast<uintptr_t>(y) & 31) == 0)
+        return deq_dispatch<true>(c, scales, nblocks, nb, fmt, layout, y, grid, st);
+    return deq_dispatch<false>(c, scales, nblocks, nb, fmt, layout, y, grid, st);
 }
+
 
 cudaError_t launch_relayout(const uint8_t* src, int src_layout, int64_t rows, int64_t cols, uint8_t* dst,
                             int dst_layout, cudaStream_t st) {

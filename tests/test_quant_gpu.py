@@ -103,18 +103,82 @@ def test_shapes_dtypes_layouts(fmt, dtype, layout):
 
 
 @pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
-def test_special_values(fmt):
-    rows, cols = 8, 64
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_special_values(fmt, dtype):
+    rows, cols = 10, 64
     x = np.zeros((rows, cols), np.float32)
     x[1, :32] = -0.0
+    x[1, 40] = -0.0
     x[2, 3] = np.nan
     x[3, 40] = np.inf
     x[4, :] = -np.inf
     x[5, :] = np.float32(2.0 ** -149) * np.arange(cols, dtype=np.float32)   # f32 subnormals
     x[6, :] = np.float32(3.0e38) * np.linspace(-1, 1, cols, dtype=np.float32)
     x[7, :] = -np.float32(1e-3)
-    codes, scales, oc, os_ = check_quantize(torch.from_numpy(x), fmt, mx.SCALES_ROWMAJOR)
+    x[8, :] = np.float32(2.0 ** -133) * np.arange(-32, 32, dtype=np.float32)  # bf16 subnormals
+    x[9, 1::2] = -0.0
+    x[9, 0::2] = -np.float32(2.0 ** -140)  # rounds to zero, keeps its sign
+    x[9, 32] = 1.0
+    xt = torch.from_numpy(x).to(dtype)
+    codes, scales, oc, os_ = check_quantize(xt, fmt, mx.SCALES_ROWMAJOR)
     assert os_[2, 0] == 0xFF and os_[3, 1] == 0xFF and os_[4, 0] == 0xFF and os_[0, 0] == 127
+
+
+def _bf16_ladder(anchor_mantissa: int) -> torch.Tensor:
+    """Blocks [anchor, v1..v31]: for the anchor 2^E (times 1 + m/128) of every
+    bf16 binade E, subnormal ones included, the v run through every bf16 bit
+    pattern of magnitude <= the anchor's, both signs (the last block of each
+    anchor is padded with +0)."""
+    out = []
+    for E in range(-133, 128):
+        a = ((E + 127) << 7 | anchor_mantissa) if E >= -126 else (1 << (E + 133))
+        pats = np.arange(0, a + 1, dtype=np.uint16)
+        pats = np.concatenate([pats, pats | 0x8000])
+        nblk = -(-len(pats) // 31)
+        flat = np.zeros(nblk * 31, np.uint16)
+        flat[:len(pats)] = pats
+        blk = np.empty((nblk, 32), np.uint16)
+        blk[:, 0] = a
+        blk[:, 1:] = flat.reshape(nblk, 31)
+        out.append(blk)
+    return torch.from_numpy(np.concatenate(out).view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
+@pytest.mark.parametrize("anchor_mantissa", [0, 0x7F])
+def test_exhaustive_bf16_elements_at_every_scale(fmt, anchor_mantissa):
+    """Every bf16 element pattern below the block maximum, at every scale a
+    bf16 block can take (the maximum 2^E or (2 - 2^-7) 2^E for every E,
+    subnormal maxima included, which also drives the scale into its -127
+    clip): codes and scales equal the oracle's, byte for byte."""
+    x = _bf16_ladder(anchor_mantissa)
+    check_quantize(x, fmt, mx.SCALES_ROWMAJOR)
+
+
+@pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
+@pytest.mark.parametrize("layout", [mx.SCALES_ROWMAJOR, mx.SCALES_MMA])
+def test_bf16_only_16_byte_aligned(fmt, layout):
+    """Input and codes that are 16- but not 32-byte aligned take the
+    four-threads-per-block path; results are the same."""
+    rng = np.random.default_rng(7)
+    rows, cols = 130, 256
+    x = torch.from_numpy(rng.standard_normal((rows, cols)).astype(np.float32)).to(torch.bfloat16)
+    big = torch.zeros(rows * cols + 8, dtype=torch.bfloat16, device="cuda")
+    xs = big[8:].view(rows, cols)
+    xs.copy_(x.cuda())
+    cb, sb = mx.mx_codes_bytes(fmt, rows, cols), mx.mx_scales_bytes(layout, rows, cols)
+    cbuf = torch.full((cb + 16 + GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+    codes = cbuf[16:16 + cb]
+    scales = torch.full((sb,), 0x5A, dtype=torch.uint8, device="cuda")
+    assert xs.data_ptr() % 32 == 16 and codes.data_ptr() % 32 == 16
+    mx.mx_quantize(xs, fmt, codes, scales, layout)
+    mx.mx_device_status()
+    oc, os_ = oracle.quantize(x.float().numpy(), O_FMT[fmt])
+    c, s = to_np(cbuf), to_np(scales)
+    assert (c[:16] == 0xA5).all() and (c[16 + cb:] == 0xA5).all()
+    assert np.array_equal(c[16:16 + cb].reshape(oc.shape), oc)
+    got_s = mma_to_rowmajor(s, rows, cols // 32) if layout == mx.SCALES_MMA else s.reshape(os_.shape)
+    assert np.array_equal(got_s, os_)
 
 
 def test_empty_is_noop():
@@ -213,7 +277,8 @@ def test_exhaustive_scale_selection(fmt):
 
 @pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
 @pytest.mark.parametrize("layout", [mx.SCALES_ROWMAJOR, mx.SCALES_MMA])
-def test_dequantize_every_code_and_scale(fmt, layout):
+@pytest.mark.parametrize("y_off", [0, 4])  # y 32-byte aligned, or only 16-byte aligned
+def test_dequantize_every_code_and_scale(fmt, layout, y_off):
     ncodes = 16 if fmt == mx.E2M1 else 256
     rows, cols = ncodes * 256, 32
     cu = np.repeat(np.arange(ncodes, dtype=np.uint8), 256)[:, None].repeat(32, axis=1)
@@ -225,13 +290,14 @@ def test_dequantize_every_code_and_scale(fmt, layout):
         s_dev = torch.from_numpy(rowmajor_to_mma(s, rows, 1)).cuda()
     else:
         s_dev = torch.from_numpy(s.copy()).cuda()
-    y = torch.full((rows * cols + 64,), 7.0, dtype=torch.float32, device="cuda")
+    ybuf = torch.full((rows * cols + 64,), 7.0, dtype=torch.float32, device="cuda")
+    y = ybuf[y_off:y_off + rows * cols]
     mx.mx_dequantize(torch.from_numpy(np.ascontiguousarray(codes)).cuda(), s_dev, rows, cols, fmt, y, layout)
     mx.mx_device_status()
-    yg = to_np(y)
-    assert (yg[rows * cols:] == 7.0).all(), "dequantize wrote past the end of y"
+    yg = to_np(ybuf)
+    assert (yg[:y_off] == 7.0).all() and (yg[y_off + rows * cols:] == 7.0).all(), "dequantize wrote outside y"
     yo = oracle.dequantize(codes, s, cols, O_FMT[fmt])
-    assert same_f32_bits(yg[:rows * cols].reshape(rows, cols), yo).all()
+    assert same_f32_bits(yg[y_off:y_off + rows * cols].reshape(rows, cols), yo).all()
 
 
 def test_dequantize_roundtrip_workload1():
