@@ -88,18 +88,19 @@ struct Work {
     int32_t tp, tq, kb0, kb1;
 };
 
-// The iter-th unit of work of this CTA; identical in every role.
-__device__ __forceinline__ bool get_work(const GemmParams& p, int iter, Work& w) {
+// The iter-th unit of work of worker `id` of `count` (a CTA, or a CTA pair);
+// identical in every role.
+__device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint32_t count, int iter, Work& w) {
     const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
     int64_t tile;
     if (p.mode == 0) {
-        tile = (int64_t)blockIdx.x + (int64_t)iter * gridDim.x;
+        tile = (int64_t)id + (int64_t)iter * count;
         if (tile >= tiles) return false;
         w.kb0 = 0;
         w.kb1 = p.k_stages;
     } else {
-        const int64_t u0 = p.total_units * blockIdx.x / gridDim.x;
-        const int64_t u1 = p.total_units * (blockIdx.x + 1) / gridDim.x;
+        const int64_t u0 = p.total_units * id / count;
+        const int64_t u1 = p.total_units * (id + 1) / count;
         if (u0 >= u1) return false;
         tile = u0 / p.k_stages + iter;
         const int64_t b = tile * p.k_stages > u0 ? tile * p.k_stages : u0;
@@ -160,6 +161,62 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
+// Write 32 rows x 128 columns of accumulator (this warp's lane quarter, in
+// registers: r[c][j] = column 32c + j of row p0 + lane) into C at (p0, qc):
+// TMA reduce-add of 32 x 16 boxes through one 2 KB 64-byte-swizzled staging
+// buffer per warp, or vector / scalar reductions.  Columns past N and rows past
+// M are clipped.
+__device__ __forceinline__ void epilogue_write_128(const GemmParams& p, const CUtensorMap& tm_c, const uint32_t (&r)[4][32],
+                                                   int32_t p0, int32_t qc, uint8_t* stage_buf, int& nbuf, int lane) {
+    const int32_t pr = p0 + lane;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (qc + 32 * c >= p.Q) break;
+        if (p.epi_red_v4) {
+            if (pr < p.P) {
+                float* row = p.C + (int64_t)pr * p.ldc + qc + 32 * c;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (qc + 32 * c + 4 * j + 3 < p.Q) {
+                        red_add_v4(row + 4 * j, __uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
+                                   __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (qc + 32 * c + 4 * j + e < p.Q) atomicAdd(row + 4 * j + e, __uint_as_float(r[c][4 * j + e]));
+                    }
+                }
+            }
+        } else if (p.use_tma_epi) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (qc + 32 * c + 16 * hh >= p.Q) break;
+                uint8_t* buf = stage_buf;  // one 32 x 16 buffer per warp
+                if (nbuf >= 1 && lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
+                // [32 rows][16 f32], 64-byte swizzle: 16-B chunk j of row i at j ^ ((i >> 1) & 3)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int js = j ^ ((lane >> 1) & 3);
+                    const uint32_t* v = &r[c][16 * hh + 4 * j];
+                    *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_2d(&tm_c, buf, qc + 32 * c + 16 * hh, p0);
+                    bulk_commit_group();
+                }
+                ++nbuf;
+            }
+        } else if (pr < p.P) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (qc + 32 * c + j < p.Q) atomicAdd(p.C + (int64_t)pr * p.ldc + qc + 32 * c + j, __uint_as_float(r[c][j]));
+        }
+    }
+}
+
 template <int KIND, int BN, int STAGES, int SWAP, int NBUF_>
 __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -217,7 +274,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         uint32_t issued_phase = 0;
         bool ok = true;
         Work w;
-        for (int it = 0; ok && get_work(p, it, w); ++it) {
+        for (int it = 0; ok && get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
             const int32_t p0 = w.tp * kBlockM;
             const int32_t q0 = w.tq * BN;
             const int nk = w.kb1 - w.kb0;
@@ -316,7 +373,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
             int sf_slot = 0;
             bool ok = true;
             Work w;
-            for (int it = 0; ok && get_work(p, it, w); ++it) {
+            for (int it = 0; ok && get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
                 const int acc = it % ACC;
                 const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
                 if (*abort_flag || !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.wait_limit_ns, err)) {
@@ -415,7 +472,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         (void)stage_buf;
         int nbuf = 0;  // chunks issued so far by this warp (buffer = nbuf % NBUF)
         Work w;
-        for (int it = 0; get_work(p, it, w); ++it) {
+        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
             const int acc = it % ACC;
             const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
             bool ok = !*abort_flag && mbar_wait(&tmem_full[acc], acc_phase, p.wait_limit_ns, err);
@@ -437,54 +494,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tmem_empty[acc]);  // TMEM free: next tile may start
-                const int32_t pr = p0 + lane;
-                const int32_t qc = q0 + h * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (qc + 32 * c >= p.Q) break;
-                    if (p.epi_red_v4) {
-                        if (pr < p.P) {
-                            float* row = p.C + (int64_t)pr * p.ldc + qc + 32 * c;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                if (qc + 32 * c + 4 * j + 3 < p.Q) {
-                                    red_add_v4(row + 4 * j, __uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
-                                               __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        if (qc + 32 * c + 4 * j + e < p.Q) atomicAdd(row + 4 * j + e, __uint_as_float(r[c][4 * j + e]));
-                                }
-                            }
-                        }
-                    } else if (p.use_tma_epi) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            if (qc + 32 * c + 16 * hh >= p.Q) break;
-                            uint8_t* buf = stage_buf;  // one 32 x 16 buffer per warp
-                            if (nbuf >= 1 && lane == 0) bulk_wait_group_read<0>();
-                            __syncwarp();
-                            // [32 rows][16 f32], 64-byte swizzle: 16-B chunk j of row i at j ^ ((i >> 1) & 3)
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int js = j ^ ((lane >> 1) & 3);
-                                const uint32_t* v = &r[c][16 * hh + 4 * j];
-                                *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = make_uint4(v[0], v[1], v[2], v[3]);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_reduce_add_2d(&tm_c, buf, qc + 32 * c + 16 * hh, p0);
-                                bulk_commit_group();
-                            }
-                            ++nbuf;
-                        }
-                    } else if (pr < p.P) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (qc + 32 * c + j < p.Q) atomicAdd(p.C + (int64_t)pr * p.ldc + qc + 32 * c + j, __uint_as_float(r[c][j]));
-                    }
-                }
+                epilogue_write_128(p, tm_c, r, p0, q0 + h * 128, stage_buf, nbuf, lane);
             } else if (SWAP) {
                 // lane i holds acc(p0 + i, q0 + j), j < BN  ->  C[q0 + j][p0 + i]
                 uint32_t r[BN];
@@ -572,6 +582,271 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------ CTA pairs
+//
+// 256 x 256 tiles on a cluster of two CTAs (tcgen05 .cta_group::2, M = 256).
+// CTA r of the pair stages rows [256 tp + 128 r, +128) of the MMA A operand
+// and rows [256 tq + 128 r, +128) of the B operand, the scale tile of its A
+// rows and the scale tiles of all 256 B rows.  Every load of both CTAs counts
+// its bytes on the even CTA's stage barrier; that CTA's MMA thread then issues
+// the scale copies and MMAs for the pair, and its commits free the stage in
+// both CTAs and hand the accumulator (rows of each CTA's half, in each CTA's
+// TMEM) to both CTAs' epilogues, whose eight warps each release it back to the
+// even CTA once drained into registers.  Per SM a stage holds 32 KB of codes
+// for the same MMA work that needs 48 KB with 128 x 256 tiles on one SM: more
+// stages fit, and a third less data crosses from L2 per MMA.
+template <int KIND, int STAGES>
+struct PairCfg {
+    static constexpr int G = KIND == KIND_F4 ? 2 : 1;  // scale groups per stage
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int A_BYTES = 128 * kRowBytes;
+    static constexpr int B_BYTES = 128 * kRowBytes;
+    static constexpr int SFA_BYTES = G * 512;
+    static constexpr int SFB_BYTES = 2 * G * 512;
+    static constexpr int SF_COLS_A = 4 * G;
+    static constexpr int SF_COLS_STAGE = 12 * G;
+    static constexpr int SF_COL0 = 256;  // accumulator in columns [0, 256)
+    static constexpr int SF_SLOTS_FIT = ((int)kTmemCols - SF_COL0) / SF_COLS_STAGE;
+    static constexpr int SF_SLOTS = SF_SLOTS_FIT < STAGES ? SF_SLOTS_FIT : STAGES;
+    static constexpr int EPI_BUF = 32 * 16 * 4;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUF;
+    static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16;
+    static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
+    static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);
+    static_assert(SF_SLOTS >= 2, "at least two scale slots in TMEM");
+    static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
+template <int KIND, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES>::THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                     const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
+    using C_ = PairCfg<KIND, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // the same offsets in both CTAs: the MMAs and barrier addresses rely on it
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C_::OFF_BAR);  // used in the even CTA
+    uint64_t* empty = full + STAGES;
+    uint64_t* tmem_full = empty + STAGES;
+    uint64_t* tmem_empty = tmem_full + 1;  // used in the even CTA
+    uint64_t* mma_done = tmem_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t pair = cluster_id_x();
+    const uint32_t npairs = cluster_count_x();
+    unsigned* err = &g_mx_device_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 2 * C_::EPI_WARPS);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
+        prefetch_tensormap(&tm_sfa);
+        prefetch_tensormap(&tm_sfb);
+        if (p.use_tma_epi) prefetch_tensormap(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA use
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t full_even = mapa_shared(smem_u32(full), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            Work w;
+            for (int it = 0; ok && get_work(p, pair, npairs, it, w); ++it) {
+                const int32_t a_row = w.tp * 256 + (int32_t)rank * 128;
+                const int32_t b_row = w.tq * 256 + (int32_t)rank * 128;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    // the even CTA announces both CTAs' bytes; a load of the odd CTA
+                    // that lands first only takes the count below zero meanwhile
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.tx_a + p.tx_b + C_::SF_TX));
+                    const uint32_t bar = full_even + (uint32_t)stage * 8;
+                    tma_load_2d_pair(smem + C_::OFF_A + stage * C_::A_BYTES, &tm_a, kb * kRowBytes, a_row, bar);
+                    tma_load_2d_pair(smem + C_::OFF_B + stage * C_::B_BYTES, &tm_b, kb * kRowBytes, b_row, bar);
+                    tma_load_3d_pair(smem + C_::OFF_SFA + stage * C_::SFA_BYTES, &tm_sfa, 0, 4 * C_::G * kb,
+                                     a_row >> 7, bar);
+                    tma_load_3d_pair(smem + C_::OFF_SFB + stage * C_::SFB_BYTES, &tm_sfb, 0, 4 * C_::G * kb,
+                                     w.tq * 2, bar);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // loads already issued count on the even CTA's barriers, which
+                // this CTA cannot wait on: give them time to land before the
+                // CTA may leave
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 100000) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (rank == 0 && lane == 0) {
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
+            const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
+            const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFB), 0, 128, 0);
+            uint32_t idesc[kMmaPerStage];
+#pragma unroll
+            for (int i = 0; i < kMmaPerStage; ++i) {
+                const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
+                idesc[i] = p.idesc | (sf_id << 4) | (sf_id << 29);
+            }
+            constexpr int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
+            constexpr int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
+            int stage = 0;
+            uint32_t phase = 0;
+            int sf_slot = 0;
+            bool ok = true;
+            Work w;
+            for (int it = 0; ok && get_work(p, pair, npairs, it, w); ++it) {
+                // both CTAs' epilogues have drained the previous tile
+                if (*abort_flag || !mbar_wait_cluster(tmem_empty, ((uint32_t)it & 1u) ^ 1u, p.wait_limit_ns, err)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
+                    if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
+                    const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
+                    const uint64_t b_desc = b_desc0 + stage * (C_::B_BYTES >> 4);
+                    const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
+                    const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
+                    // scale tiles -> TMEM: A group g at sf_col + 4g; B group g, row tile t
+                    // at sf_col + SF_COLS_A + 4 (2g + t)
+#pragma unroll
+                    for (int g = 0; g < C_::G; ++g) {
+                        tc_cp_pair_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
+#pragma unroll
+                        for (int t = 0; t < 2; ++t)
+                            tc_cp_pair_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (2 * g + t),
+                                                      sfb_desc + (t * C_::G + g) * 32);
+                    }
+                    const int rem = p.K - kb * k_elem_per_stage;
+                    if (rem >= k_elem_per_stage) {
+#pragma unroll
+                        for (int i = 0; i < kMmaPerStage; ++i) {
+                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
+                            if (KIND == KIND_F4)
+                                mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                              sf_col + C_::SF_COLS_A + 8 * g, accum);
+                            else
+                                mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
+                        }
+                    } else {
+                        // the ragged last stage of K
+                        const int n_mma = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
+                        for (int i = 0; i < n_mma; ++i) {
+                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                            const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
+                            const uint32_t id = p.idesc | (sf_id << 4) | (sf_id << 29);
+                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
+                            if (KIND == KIND_F4)
+                                mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
+                                              sf_col + C_::SF_COLS_A + 8 * g, accum);
+                            else
+                                mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
+                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
+                        }
+                    }
+                    tc_commit_pair(&empty[stage]);  // stage free in both CTAs once read
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair(tmem_full);
+            }
+            // every tcgen05 op issued for the pair completes before TMEM is freed
+            tc_commit_pair(mma_done);
+            mbar_wait(mma_done, 0, p.wait_limit_ns, err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;         // TMEM lane quarter this warp may read
+        const int h = (warp - 2) >> 2;  // which 128 of the 256 columns
+        uint8_t* stage_buf = smem + C_::OFF_EPI + (warp - 2) * C_::EPI_BUF;
+        const uint32_t tmem_empty_even = mapa_shared(smem_u32(tmem_empty), 0);
+        int nbuf = 0;
+        Work w;
+        for (int it = 0; get_work(p, pair, npairs, it, w); ++it) {
+            const bool ok = !*abort_flag && mbar_wait_cluster(tmem_full, (uint32_t)it & 1u, p.wait_limit_ns, err);
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int32_t p0 = w.tp * 256 + (int32_t)rank * 128 + 32 * q;
+            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + h * 128;
+            uint32_t r[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_row + 32 * c, r[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(tmem_empty_even);  // next tile's MMAs may start
+            epilogue_write_128(p, tm_c, r, p0, w.tq * 256 + h * 128, stage_buf, nbuf, lane);
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the even CTA's MMAs no longer read or write this CTA
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -642,7 +917,7 @@ bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_co
 // Instruction descriptor (block-scaled kinds), scale-factor ids left 0:
 //   [7,10) A type  [10,13) B type  [15] A K-major(0)  [16] B K-major(0)
 //   [17,23) N>>3   [23] scale type UE8M0 (1)   [24,29) M>>4
-uint32_t make_idesc(int kind, int a_fmt, int b_fmt, int n) {
+uint32_t make_idesc(int kind, int a_fmt, int b_fmt, int n, int m = kBlockM) {
     auto code = [&](int f) -> uint32_t {
         if (kind == KIND_F4) return 1u;          // E2M1 in kind::mxf4
         return f == FMT_E2M1 ? 5u : 0u;          // kind::mxf8f6f4: E2M1 = 5, E4M3 = 0
@@ -652,8 +927,24 @@ uint32_t make_idesc(int kind, int a_fmt, int b_fmt, int n) {
     d |= code(b_fmt) << 10;
     d |= (uint32_t)(n >> 3) << 17;
     d |= 1u << 23;
-    d |= (uint32_t)(kBlockM >> 4) << 24;
+    d |= (uint32_t)(m >> 4) << 24;
     return d;
+}
+
+// Tensor map over scales in the tensor-core layout, as [tiles][4 * groups][128 B]
+// (a 128-row tile's group g is the 512 bytes of rows 4g .. 4g+3): a box of
+// 4 * g_box rows x `tiles_box` tiles loads g_box groups of that many tiles.
+bool make_sf_map(CUtensorMap* m, const uint8_t* sf, int64_t rows, int32_t sf_groups, int g_box, int tiles_box) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)sf_groups * 4, (cuuint64_t)((rows + 127) / 128)};
+    cuuint64_t strides[2] = {128, (cuuint64_t)sf_groups * 512};
+    cuuint32_t box[3] = {128, (cuuint32_t)(4 * g_box), (cuuint32_t)tiles_box};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(sf), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0>
@@ -669,6 +960,44 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     }
     kern<<<grid, C_::THREADS, C_::SMEM, st>>>(ta, tb, tc, p);
     return cudaGetLastError();
+}
+
+// CTA pairs that can be resident at once for a pair-kernel instantiation
+// (pairs need two SMs of one GPU processing cluster); cached per instantiation.
+template <int KIND, int STAGES>
+cudaError_t run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
+                     const CUtensorMap& tc, const GemmParams& p, int pairs, cudaStream_t st) {
+    using C_ = PairCfg<KIND, STAGES>;
+    auto kern = gemm_pair_kernel<KIND, STAGES>;
+    kern<<<2 * pairs, C_::THREADS, C_::SMEM, st>>>(ta, tb, tsa, tsb, tc, p);
+    return cudaGetLastError();
+}
+
+template <int KIND, int STAGES>
+int pair_capacity() {
+    using C_ = PairCfg<KIND, STAGES>;
+    static int cap = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        auto kern = gemm_pair_kernel<KIND, STAGES>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM) != cudaSuccess) {
+            cudaGetLastError();
+            cap = 0;
+            return;
+        }
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2), 1, 1);
+        cfg.blockDim = dim3(C_::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = C_::SMEM;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cap = n;
+    });
+    return cap;
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns) {
@@ -688,6 +1017,61 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+namespace {
+
+// 256 x 256 tiles on CTA pairs.  Returns cudaErrorNotSupported (nothing
+// launched) when no pair can be resident, so the caller takes the one-CTA path.
+cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const uint8_t* x_sf, int x_fmt, int64_t P,
+                        const void* y_codes, const uint8_t* y_sf, int y_fmt, int64_t Q, cudaStream_t st,
+                        const char** detail) {
+    const int cap = kind == KIND_F4 ? pair_capacity<KIND_F4, 5>() : pair_capacity<KIND_F8F6F4, 6>();
+    if (cap <= 0) return cudaErrorNotSupported;
+    const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
+    const int g = kind == KIND_F4 ? 2 : 1;
+    auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.P = (int32_t)P;
+    p.Q = (int32_t)Q;
+    p.K = (int32_t)a.K;
+    p.tiles_p = (int32_t)((P + 255) / 256);
+    p.tiles_q = (int32_t)((Q + 255) / 256);
+    p.k_stages = (int32_t)((a.K + k_per_stage - 1) / k_per_stage);
+    p.sf_groups = (int32_t)(round_up(a.K / 32, 4) / 4);
+    p.wait_limit_ns = wait_limit_ns();
+    p.idesc = make_idesc(kind, x_fmt, y_fmt, 256, 256);
+    p.use_tma_epi = (a.N % 4) == 0 ? 1 : 0;
+    p.C = a.C;
+    p.ldc = a.N;
+    p.sfa = x_sf;
+    p.sfb = y_sf;
+    p.tx_a = 128u * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.tx_b = 128u * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.nb = (int32_t)(a.K / 32);
+    CUtensorMap ta, tb, tsa, tsb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    if (!make_operand_map(&ta, x_codes, P, a.K, fk(x_fmt), 128) || !make_operand_map(&tb, y_codes, Q, a.K, fk(y_fmt), 128) ||
+        !make_sf_map(&tsa, x_sf, P, p.sf_groups, g, 1) || !make_sf_map(&tsb, y_sf, Q, p.sf_groups, g, 2) ||
+        (p.use_tma_epi && !make_c_map(&tc, a.C, a.M, a.N, 16, 32, 64))) {
+        *detail = "cuTensorMapEncodeTiled rejected an operand";
+        return cudaErrorInvalidValue;
+    }
+    const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
+    p.total_units = tiles * p.k_stages;
+    int pairs;
+    if (tiles >= cap || p.k_stages < 4) {
+        p.mode = 0;
+        pairs = (int)(tiles < cap ? tiles : cap);
+    } else {
+        p.mode = 1;  // slices of (tile, stage) per pair
+        pairs = (int)(p.total_units < cap ? p.total_units : cap);
+    }
+    if (kind == KIND_F4) return run_pair<KIND_F4, 5>(ta, tb, tsa, tsb, tc, p, pairs, st);
+    return run_pair<KIND_F8F6F4, 6>(ta, tb, tsa, tsb, tc, p, pairs, st);
+}
+
+}  // namespace
+
 cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char** detail) {
     *detail = nullptr;
     const bool swap = a.M <= 64 && a.N > a.M;
@@ -703,6 +1087,11 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
 
     const int kind = (x_fmt == FMT_E2M1 && y_fmt == FMT_E2M1) ? KIND_F4 : KIND_F8F6F4;
     const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
+
+    if (!swap && P > 128 && Q > 128 && a.scale_layout == LAYOUT_MMA) {
+        cudaError_t e = launch_pair(a, kind, x_codes, x_sf, x_fmt, P, y_codes, y_sf, y_fmt, Q, st, detail);
+        if (e != cudaErrorNotSupported) return e;
+    }
 
     int bn;
     if (swap) {

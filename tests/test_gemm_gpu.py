@@ -133,6 +133,22 @@ def test_ragged_shapes(M, N, K, fa, fb):
     run_full(randn(rng, (M, K)), randn(rng, (N, K)), fa, fb, randn(rng, (M, N)))
 
 
+# ------------------------------------------------ 256 x 256 tiles on CTA pairs
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (512, 512, 1024, mx.E4M3FN, mx.E4M3FN),
+    (300, 600, 416, mx.E2M1, mx.E2M1),       # ragged K with an odd count of 4-block scale groups
+    (260, 1000, 384, mx.E4M3FN, mx.E2M1),    # the odd CTA's A rows mostly past M
+    (520, 260, 1152, mx.E2M1, mx.E4M3FN),    # the odd CTA's B rows mostly past N (mixed: K % 128 == 0)
+    (129, 129, 64, mx.E4M3FN, mx.E4M3FN),    # N % 4 != 0 (per-element epilogue), K shorter than a stage
+    (1024, 768, 2048, mx.E2M1, mx.E2M1),     # few tiles, K split across pairs
+    (2048, 2048, 256, mx.E4M3FN, mx.E4M3FN), # several tiles per pair
+])
+def test_pair_tiles(M, N, K, fa, fb):
+    rng = np.random.default_rng(M * 5 + N * 11 + K)
+    run_full(randn(rng, (M, K)), randn(rng, (N, K)), fa, fb, randn(rng, (M, N)))
+
+
 # ------------------------------------------------------ row-major scales
 
 @pytest.mark.parametrize("M,N,K,fa,fb", [
