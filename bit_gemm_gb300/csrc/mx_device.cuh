@@ -69,6 +69,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition.  A thread that issues tensor-core
+// work tests the NEXT stage's barrier ahead of time and branches on the answer
+// only a stage later: the test's latency then overlaps the issue instead of
+// stalling it (a dependent shared-memory round trip per stage leaves the MMA
+// pipe idle for its duration).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (and raises MX_DEVERR_TIMEOUT in *err) when `limit_ns` elapses first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, unsigned* err) {
@@ -82,6 +99,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
             return false;
         }
     }
+}
+
+// ----------------------------------------------------------- named barriers
+//
+// Hardware CTA barriers 1..15 (0 is __syncthreads), executed by whole warps.
+// A warp that issues tensor-core work learns that a stage is ready through
+// one of these instead of an mbarrier: any shared-memory access by the issuing
+// thread stalls its tcgen05 issue for the access's round trip, a named barrier
+// does not.  They have no timeout, so the two warps that share one sync on it
+// in lockstep, the same number of times on every path.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- fences

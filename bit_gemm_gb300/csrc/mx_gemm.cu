@@ -384,13 +384,21 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + kAccCol + acc * BN;
                 const int nk = w.kb1 - w.kb0;
+                bool ready = mbar_test_wait(&full[stage], phase);
                 for (int j = 0; j < nk; ++j) {
                     const int kb = w.kb0 + j;
-                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
+                    if (!ready && !mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
+                    int next_stage = stage + 1;
+                    uint32_t next_phase = phase;
+                    if (next_stage == STAGES) {
+                        next_stage = 0;
+                        next_phase ^= 1;
+                    }
+                    ready = mbar_test_wait(&full[next_stage], next_phase);  // used one stage later
                     tc_fence_after();
                     // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
                     // through the async proxy
@@ -453,10 +461,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                         }
                     }
                     tc_commit(&empty[stage]);  // stage free once these MMAs have read it
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
+                    stage = next_stage;
+                    phase = next_phase;
                 }
                 if (!ok) break;
                 tc_commit(&tmem_full[acc]);
@@ -592,14 +598,18 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
 // the scale copies and MMAs for the pair, and its commits free the stage in
 // both CTAs and hand the accumulator (rows of each CTA's half, in each CTA's
 // TMEM) to both CTAs' epilogues, whose eight warps each release it back to the
-// even CTA once drained into registers.  Per SM a stage holds 32 KB of codes
+// even CTA once drained into registers.  In the even CTA a gate warp waits on
+// each stage's barrier and passes it to the MMA warp through a named barrier
+// (one per stage slot), so the issuing thread never touches shared memory
+// between MMAs.  Per SM a stage holds 32 KB of codes
 // for the same MMA work that needs 48 KB with 128 x 256 tiles on one SM: more
 // stages fit, and a third less data crosses from L2 per MMA.
 template <int KIND, int STAGES>
 struct PairCfg {
     static constexpr int G = KIND == KIND_F4 ? 2 : 1;  // scale groups per stage
     static constexpr int EPI_WARPS = 8;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
+    static constexpr int THREADS = 32 * (GATE_WARP + 1);
     static constexpr int A_BYTES = 128 * kRowBytes;
     static constexpr int B_BYTES = 128 * kRowBytes;
     static constexpr int SFA_BYTES = G * 512;
@@ -621,6 +631,7 @@ struct PairCfg {
     static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);
     static_assert(SF_SLOTS >= 2, "at least two scale slots in TMEM");
     static_assert(SMEM <= 232448, "shared memory per CTA");
+    static_assert(STAGES <= 15, "one named barrier per stage");
 };
 
 template <int KIND, int STAGES>
@@ -718,7 +729,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (rank == 0 && lane == 0) {
+        // The whole warp walks the schedule and syncs on stage s's named
+        // barrier (1 + s) with the gate warp; lane 0 issues.  After an abort
+        // the warp keeps walking (and syncing) without issuing, so its syncs
+        // and the gate's always pair up.
+        if (rank == 0) {
             const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
             const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
             const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
@@ -732,84 +747,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
             constexpr int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
             constexpr int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
             int stage = 0;
-            uint32_t phase = 0;
             int sf_slot = 0;
-            bool ok = true;
+            bool live = true;  // false after an abort: walk without issuing
             Work w;
-            for (int it = 0; ok && get_work(p, pair, npairs, it, w); ++it) {
+            for (int it = 0; get_work(p, pair, npairs, it, w); ++it) {
                 // both CTAs' epilogues have drained the previous tile
-                if (*abort_flag || !mbar_wait_cluster(tmem_empty, ((uint32_t)it & 1u) ^ 1u, p.wait_limit_ns, err)) {
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
+                int okt = 1;
+                if (lane == 0 && live)
+                    okt = !*abort_flag && mbar_wait_cluster(tmem_empty, ((uint32_t)it & 1u) ^ 1u, p.wait_limit_ns, err);
+                okt = __shfl_sync(0xFFFFFFFFu, okt, 0);
+                if (live && !okt) {
+                    live = false;
+                    if (lane == 0) *abort_flag = 1;
                 }
-                tc_fence_after();
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
+                    named_bar_sync(1 + stage, 64);  // the gate saw this stage's data land
+                    if (lane == 0 && live) {
+                        tc_fence_after();
+                        const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
+                        const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
+                        const uint64_t b_desc = b_desc0 + stage * (C_::B_BYTES >> 4);
+                        const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
+                        const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
+                        // scale tiles -> TMEM: A group g at sf_col + 4g; B group g, row tile t
+                        // at sf_col + SF_COLS_A + 4 (2g + t)
+#pragma unroll
+                        for (int g = 0; g < C_::G; ++g) {
+                            tc_cp_pair_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
+#pragma unroll
+                            for (int t = 0; t < 2; ++t)
+                                tc_cp_pair_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (2 * g + t),
+                                                          sfb_desc + (t * C_::G + g) * 32);
+                        }
+                        const int rem = p.K - kb * k_elem_per_stage;
+                        if (rem >= k_elem_per_stage) {
+#pragma unroll
+                            for (int i = 0; i < kMmaPerStage; ++i) {
+                                const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                                const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
+                                if (KIND == KIND_F4)
+                                    mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
+                                else
+                                    mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                                                      sf_col + C_::SF_COLS_A + 8 * g, accum);
+                            }
+                        } else {
+                            // the ragged last stage of K
+                            const int n_mma = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
+                            for (int i = 0; i < n_mma; ++i) {
+                                const int g = KIND == KIND_F4 ? (i >> 1) : 0;
+                                const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
+                                const uint32_t id = p.idesc | (sf_id << 4) | (sf_id << 29);
+                                const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
+                                if (KIND == KIND_F4)
+                                    mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
+                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
+                                else
+                                    mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
+                                                      sf_col + C_::SF_COLS_A + 8 * g, accum);
+                            }
+                        }
+                        tc_commit_pair(&empty[stage]);  // stage free in both CTAs once read
                     }
-                    tc_fence_after();
-                    const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
+                    __syncwarp();
                     if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
-                    const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
-                    const uint64_t b_desc = b_desc0 + stage * (C_::B_BYTES >> 4);
-                    const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
-                    const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
-                    // scale tiles -> TMEM: A group g at sf_col + 4g; B group g, row tile t
-                    // at sf_col + SF_COLS_A + 4 (2g + t)
-#pragma unroll
-                    for (int g = 0; g < C_::G; ++g) {
-                        tc_cp_pair_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
-#pragma unroll
-                        for (int t = 0; t < 2; ++t)
-                            tc_cp_pair_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (2 * g + t),
-                                                      sfb_desc + (t * C_::G + g) * 32);
-                    }
-                    const int rem = p.K - kb * k_elem_per_stage;
-                    if (rem >= k_elem_per_stage) {
-#pragma unroll
-                        for (int i = 0; i < kMmaPerStage; ++i) {
-                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
-                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
-                            if (KIND == KIND_F4)
-                                mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
-                                              sf_col + C_::SF_COLS_A + 8 * g, accum);
-                            else
-                                mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
-                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
-                        }
-                    } else {
-                        // the ragged last stage of K
-                        const int n_mma = (rem + k_elem_per_mma - 1) / k_elem_per_mma;
-                        for (int i = 0; i < n_mma; ++i) {
-                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
-                            const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
-                            const uint32_t id = p.idesc | (sf_id << 4) | (sf_id << 29);
-                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
-                            if (KIND == KIND_F4)
-                                mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
-                                              sf_col + C_::SF_COLS_A + 8 * g, accum);
-                            else
-                                mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
-                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
+                    if (++stage == STAGES) stage = 0;
+                }
+                if (lane == 0 && live) tc_commit_pair(tmem_full);
+                __syncwarp();
+            }
+            if (lane == 0) {
+                // every tcgen05 op issued for the pair completes before TMEM is freed
+                tc_commit_pair(mma_done);
+                mbar_wait(mma_done, 0, p.wait_limit_ns, err);
+            }
+            __syncwarp();
+        }
+    } else if (warp == C_::GATE_WARP) {
+        // ---------------------------------------------------------------- gate
+        // Even CTA: for every stage of the schedule, wait (bounded) for its
+        // data, then sync with the MMA warp on the stage's named barrier.  The
+        // two warps sync once per stage in the same order (lockstep: neither
+        // can run a generation ahead), and after a timeout the gate stops
+        // waiting but keeps syncing, so every sync has its partner.  The
+        // gate's wait for stage s + 1 overlaps the MMA warp's issue of stage
+        // s, which the tensor pipe paces.
+        if (rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool live = true;
+            Work w;
+            for (int it = 0; get_work(p, pair, npairs, it, w); ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (live) {
+                        int okw = 1;
+                        if (lane == 0) okw = mbar_wait(&full[stage], phase, p.wait_limit_ns, err);
+                        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                        if (!okw) {
+                            live = false;
+                            if (lane == 0) *abort_flag = 1;
                         }
                     }
-                    tc_commit_pair(&empty[stage]);  // stage free in both CTAs once read
+                    named_bar_sync(1 + stage, 64);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
-                if (!ok) break;
-                tc_commit_pair(tmem_full);
             }
-            // every tcgen05 op issued for the pair completes before TMEM is freed
-            tc_commit_pair(mma_done);
-            mbar_wait(mma_done, 0, p.wait_limit_ns, err);
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;         // TMEM lane quarter this warp may read
