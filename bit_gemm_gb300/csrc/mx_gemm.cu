@@ -126,7 +126,8 @@ struct Cfg {
     // the next tile's MMAs overlap the write-out of this one
     static constexpr int ACC = (!SWAP && 2 * BN <= 256) ? 2 : 1;
     static constexpr int EPI_WARPS = (!SWAP && BN == 256) ? 8 : 4;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
+    static constexpr int THREADS = 32 * (GATE_WARP + 1);
     static constexpr int A_BYTES = kBlockM * kRowBytes;               // 16 KB
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int SFA_BYTES = G * 512;
@@ -159,6 +160,7 @@ struct Cfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
+    static_assert(STAGES <= 15, "one named barrier per stage");
 };
 
 // Write 32 rows x 128 columns of accumulator (this warp's lane quarter, in
@@ -351,68 +353,58 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            // Everything that does not depend on the stage is built once: the
-            // shared-memory descriptors of stage 0 (a stage's descriptors differ
-            // only in the start-address field, which is advanced by adds) and
-            // the four instruction descriptors carrying the scale-factor ids.
-            const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
-            const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
-            const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
-            const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFB), 0, 128, 0);
-            uint32_t idesc[kMmaPerStage];
+        // The whole warp walks the schedule and syncs on stage s's named
+        // barrier (1 + s) with the gate warp, which has seen the stage's data
+        // land; lane 0 issues.  After an abort the warp keeps walking (and
+        // syncing) without issuing, so its syncs and the gate's always pair up.
+        // Everything that does not depend on the stage is built once: the
+        // shared-memory descriptors of stage 0 (a stage's descriptors differ
+        // only in the start-address field, which is advanced by adds) and the
+        // four instruction descriptors carrying the scale-factor ids.
+        const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
+        const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
+        const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
+        const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFB), 0, 128, 0);
+        uint32_t idesc[kMmaPerStage];
 #pragma unroll
-            for (int i = 0; i < kMmaPerStage; ++i) {
-                // kind::mxf4: MMA i covers blocks 2i, 2i+1 of the stage (scale bytes
-                // 0-1 or 2-3 of its group); kind::mxf8f6f4: block i (byte i)
-                const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
-                idesc[i] = p.idesc | (sf_id << 4) | (sf_id << 29);
+        for (int i = 0; i < kMmaPerStage; ++i) {
+            // kind::mxf4: MMA i covers blocks 2i, 2i+1 of the stage (scale bytes
+            // 0-1 or 2-3 of its group); kind::mxf8f6f4: block i (byte i)
+            const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
+            idesc[i] = p.idesc | (sf_id << 4) | (sf_id << 29);
+        }
+        constexpr int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
+        constexpr int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
+        int stage = 0;
+        int sf_slot = 0;
+        bool live = true;  // false after an abort: walk without issuing
+        Work w;
+        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+            const int acc = it % ACC;
+            const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
+            int okt = 1;
+            if (lane == 0 && live)
+                okt = !*abort_flag && mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.wait_limit_ns, err);
+            okt = __shfl_sync(0xFFFFFFFFu, okt, 0);
+            if (live && !okt) {
+                live = false;
+                if (lane == 0) *abort_flag = 1;
             }
-            int stage = 0;
-            uint32_t phase = 0;
-            int sf_slot = 0;
-            bool ok = true;
-            Work w;
-            for (int it = 0; ok && get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
-                const int acc = it % ACC;
-                const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
-                if (*abort_flag || !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.wait_limit_ns, err)) {
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + kAccCol + acc * BN;
-                const int nk = w.kb1 - w.kb0;
-                bool ready = mbar_test_wait(&full[stage], phase);
-                for (int j = 0; j < nk; ++j) {
-                    const int kb = w.kb0 + j;
-                    if (!ready && !mbar_wait(&full[stage], phase, p.wait_limit_ns, err)) {
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    int next_stage = stage + 1;
-                    uint32_t next_phase = phase;
-                    if (next_stage == STAGES) {
-                        next_stage = 0;
-                        next_phase ^= 1;
-                    }
-                    ready = mbar_test_wait(&full[next_stage], next_phase);  // used one stage later
+            const uint32_t d_tmem = tmem + kAccCol + acc * BN;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                named_bar_sync(1 + stage, 64);  // the gate saw this stage's data land
+                if (lane == 0 && live) {
                     tc_fence_after();
                     // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
                     // through the async proxy
                     if (p.sf_rowmajor) fence_proxy_async_smem();
                     const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
-                    if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
                     const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
                     const uint64_t b_desc = b_desc0 + stage * (C_::B_BYTES >> 4);
                     const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
                     const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
                     const int g_first = kb * C_::G;
                     // valid MMAs in this stage (ragged K): each consumes 32 bytes of K
-                    const int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
-                    const int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
                     const int rem = p.K - kb * k_elem_per_stage;
                     if (rem >= k_elem_per_stage) {
                         // full stage: everything unrolled.
@@ -429,7 +421,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
 #pragma unroll
                         for (int i = 0; i < kMmaPerStage; ++i) {
                             const int g = KIND == KIND_F4 ? (i >> 1) : 0;
-                            const uint32_t accum = (j > 0 || i > 0) ? 1u : 0u;
+                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
                             if (KIND == KIND_F4)
                                 mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
                                          sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
@@ -451,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                             const int g = KIND == KIND_F4 ? (i >> 1) : 0;
                             const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
                             const uint32_t id = p.idesc | (sf_id << 4) | (sf_id << 29);
-                            const uint32_t accum = (j > 0 || i > 0) ? 1u : 0u;
+                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
                             if (KIND == KIND_F4)
                                 mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, id, sf_col + 4 * g,
                                          sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
@@ -461,15 +453,47 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                         }
                     }
                     tc_commit(&empty[stage]);  // stage free once these MMAs have read it
-                    stage = next_stage;
-                    phase = next_phase;
                 }
-                if (!ok) break;
-                tc_commit(&tmem_full[acc]);
+                __syncwarp();
+                if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
+                if (++stage == STAGES) stage = 0;
             }
+            if (lane == 0 && live) tc_commit(&tmem_full[acc]);
+            __syncwarp();
+        }
+        if (lane == 0) {
             // every tcgen05 op issued by this thread completes before TMEM is freed
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, p.wait_limit_ns, err);
+        }
+        __syncwarp();
+    } else if (warp == C_::GATE_WARP) {
+        // ---------------------------------------------------------------- gate
+        // For every stage of the schedule, wait (bounded) for its data, then
+        // sync with the MMA warp on the stage's named barrier: once per stage,
+        // in the same order, so neither warp can run a generation ahead; after
+        // a timeout the gate stops waiting but keeps syncing.
+        int stage = 0;
+        uint32_t phase = 0;
+        bool live = true;
+        Work w;
+        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                if (live) {
+                    int okw = 1;
+                    if (lane == 0) okw = mbar_wait(&full[stage], phase, p.wait_limit_ns, err);
+                    okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                    if (!okw) {
+                        live = false;
+                        if (lane == 0) *abort_flag = 1;
+                    }
+                }
+                named_bar_sync(1 + stage, 64);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
