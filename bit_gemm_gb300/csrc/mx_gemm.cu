@@ -82,6 +82,7 @@ struct GemmParams {
     uint32_t tx_a, tx_b;   // bytes one stage's code load counts on its barrier
     int32_t sf_rowmajor;   // 1: scales are row-major [rows][K/32]; gathered by the producer lanes
     int32_t nb;            // K / 32 (row stride of row-major scales, a multiple of 4)
+    int32_t group_p;       // whole-tile order: bands of this many row tiles sweep all column tiles
 };
 
 struct Work {
@@ -98,6 +99,15 @@ __device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint3
         if (tile >= tiles) return false;
         w.kb0 = 0;
         w.kb1 = p.k_stages;
+        // bands of group_p row tiles: within a band the row tile varies fastest,
+        // so the band's A rows stay in L2 while its column tiles stream past
+        const int64_t band_tiles = (int64_t)p.group_p * p.tiles_q;
+        const int64_t band = tile / band_tiles;
+        const int64_t r = tile - band * band_tiles;
+        const int64_t rows_in_band = min((int64_t)p.group_p, (int64_t)p.tiles_p - band * p.group_p);
+        w.tp = (int32_t)(band * p.group_p + r % rows_in_band);
+        w.tq = (int32_t)(r / rows_in_band);
+        return true;
     } else {
         const int64_t u0 = p.total_units * id / count;
         const int64_t u1 = p.total_units * (id + 1) / count;
@@ -1090,6 +1100,17 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t st) {
 
 namespace {
 
+// Row tiles per band of the whole-tile order: as many as keep the band's A
+// codes within about 40 MB (a third of L2, which C's read-modify-write traffic
+// also passes through), so they are read from HBM once while every column
+// tile streams past; all row tiles when A fits.
+int32_t band_rows(int32_t tiles_p, int64_t a_tile_bytes) {
+    const int64_t budget = 40ll << 20;
+    int64_t g = a_tile_bytes > 0 ? budget / a_tile_bytes : tiles_p;
+    if (g < 1) g = 1;
+    return (int32_t)(g < tiles_p ? g : tiles_p);
+}
+
 // 256 x 256 tiles on CTA pairs.  Returns cudaErrorNotSupported (nothing
 // launched) when no pair can be resident, so the caller takes the one-CTA path.
 cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const uint8_t* x_sf, int x_fmt, int64_t P,
@@ -1129,6 +1150,7 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     }
     const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
     p.total_units = tiles * p.k_stages;
+    p.group_p = band_rows(p.tiles_p, 256 * (x_fmt == FMT_E2M1 ? a.K / 2 : a.K));
     int pairs;
     if (tiles >= cap || p.k_stages < 4) {
         p.mode = 0;
@@ -1216,6 +1238,7 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     p.nb = (int32_t)(a.K / 32);
     const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
     p.total_units = tiles * p.k_stages;
+    p.group_p = band_rows(p.tiles_p, kBlockM * (x_fmt == FMT_E2M1 ? a.K / 2 : a.K));
     const int sms = sm_count();
     int grid;
     if (tiles >= sms || p.k_stages < 4) {
