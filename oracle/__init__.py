@@ -41,6 +41,16 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.mxo_decode_scale.restype = dbl
     L.mxo_floor_log2.argtypes = [dbl]
     L.mxo_floor_log2.restype = i32
+    L.mxo_quantize_axis0.argtypes = [vp, i64, i64, i32, vp, vp]
+    L.mxo_quantize_axis0.restype = i32
+    L.mxo_dequantize_bf16.argtypes = [vp, vp, i64, i64, i32, vp]
+    L.mxo_dequantize_bf16.restype = i32
+    L.mxo_block_matmul_f32b.argtypes = [vp, vp, i32, vp, i64, i64, i64, vp, vp, vp]
+    L.mxo_block_matmul_f32b.restype = i32
+    L.mxo_fold_scale.argtypes = [vp, i64, i32]
+    L.mxo_fold_scale.restype = None
+    L.mxo_fold_exponent.argtypes = [dbl]
+    L.mxo_fold_exponent.restype = i32
     L.mxo_num_threads.argtypes = []
     L.mxo_num_threads.restype = i32
     L.mxo_set_num_threads.argtypes = [i32]
@@ -145,6 +155,60 @@ def block_matmul_entries(a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, K,
     if rc:
         raise ValueError("oracle block_matmul_entries rejected shape/format")
     return ref, sabs
+
+
+def quantize_axis0(x: np.ndarray, fmt: int) -> tuple[np.ndarray, np.ndarray]:
+    """x: float32 [rows, cols], blocks of 32 rows down each column ->
+    (codes uint8 [cols, cb(rows)], scales uint8 [cols, rows/32]): the layout of
+    the transposed tensor."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    codes = np.zeros((cols, code_bytes_per_row(fmt, rows)), np.uint8)
+    scales = np.zeros((cols, rows // BLOCK), np.uint8)
+    rc = lib().mxo_quantize_axis0(_ptr(x), rows, cols, fmt, _ptr(codes), _ptr(scales))
+    if rc:
+        raise ValueError(f"oracle quantize_axis0 rejected shape/format (rc={rc})")
+    return codes, scales
+
+
+def dequantize_bf16(codes: np.ndarray, scales: np.ndarray, cols: int, fmt: int) -> np.ndarray:
+    """-> uint16 [rows, cols]: bfloat16 bit patterns."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows = scales.shape[0]
+    y = np.zeros((rows, cols), np.uint16)
+    rc = lib().mxo_dequantize_bf16(_ptr(codes), _ptr(scales), rows, cols, fmt, _ptr(y))
+    if rc:
+        raise ValueError(f"oracle dequantize_bf16 rejected shape/format (rc={rc})")
+    return y
+
+
+def block_matmul_f32b(a_codes, a_scales, a_fmt, B, M, N, K, c0):
+    """C0 + deq(A) . B with B f32 [K, N] row-major; returns (ref, sabs) f64 [M, N]."""
+    a_codes = np.ascontiguousarray(a_codes, np.uint8)
+    a_scales = np.ascontiguousarray(a_scales, np.uint8)
+    B = np.ascontiguousarray(B, np.float32)
+    c0 = np.ascontiguousarray(c0, np.float32)
+    ref = np.zeros((M, N), np.float64)
+    sabs = np.zeros((M, N), np.float64)
+    rc = lib().mxo_block_matmul_f32b(_ptr(a_codes), _ptr(a_scales), a_fmt, _ptr(B), M, N, K, _ptr(c0),
+                                     _ptr(ref), _ptr(sabs))
+    if rc:
+        raise ValueError("oracle block_matmul_f32b rejected shape/format")
+    return ref, sabs
+
+
+def fold_scale(scales: np.ndarray, j: int) -> np.ndarray:
+    """A copy of the scale bytes with the power-of-two factor 2^j folded in."""
+    out = np.ascontiguousarray(scales, dtype=np.uint8).copy()
+    lib().mxo_fold_scale(_ptr(out), out.size, int(j))
+    return out
+
+
+def fold_exponent(scalar: float):
+    """j for a foldable scalar 2^j, else None."""
+    j = lib().mxo_fold_exponent(float(scalar))
+    return None if j == -1000 else j
 
 
 def decode_element(fmt: int, code: int) -> float:

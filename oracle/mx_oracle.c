@@ -26,6 +26,15 @@
  *   R4 a block holding a NaN or an infinity gets scale 0xFF and codes 0.
  *   R5 scale bytes for the GEMM are exact powers of two; products are formed
  *      from the exact dequantized values in binary64.
+ *   R6 quantizing along the first axis writes its outputs in the layout of
+ *      the transposed tensor ([N, K] codes and scales), the operand layout of
+ *      block_matmul.
+ *   R7 dequantize to bfloat16 is the exact value rounded to nearest, ties to
+ *      even (the IEEE conversion; the pages name only the output type).
+ *   R8 the f32 right-hand operand of the pages' first block_matmul is
+ *      row-major [K, N].
+ *   R9 fold_scale accepts only a positive finite power of two 2^j; the scale
+ *      byte saturates at 0 and 254 and 0xFF stays 0xFF.
  *
  * Parity pins for every function here live in tests/test_oracle_pins.py.
  *
@@ -349,6 +358,147 @@ int mxo_block_matmul_entries(const uint8_t* a_codes, const uint8_t* a_scales, in
         matmul_entry(a_fmt, a_codes, a_scales, b_fmt, b_codes, b_scales, K, a_row[i], b_row[i],
                      (double)c0[i], &ref[i], &sabs[i]);
     return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * The block axis ([Dialect] "The block axis"): blocking is along the reduction
+ * axis, which for the right-hand operand of a product is its FIRST axis.
+ * Quantize a row-major [rows, cols] tensor in blocks of 32 consecutive rows of
+ * one column.  The outputs are laid out as the transposed tensor's would be:
+ * codes [cols, rows] (row c holds column c's codes, packed as usual) and scales
+ * [cols, rows/32], so that the result is directly a [N, K] operand.
+ * Returns 0, 1 (bad shape: rows % 32 != 0) or 2 (bad format).
+ * ------------------------------------------------------------------------- */
+int mxo_quantize_axis0(const float* x, int64_t rows, int64_t cols, int fmt,
+                       uint8_t* codes, uint8_t* scales)
+{
+    int rc = check_shape(fmt, cols, rows);
+    if (rc) return rc;
+    const int64_t nb = rows / MXO_BLOCK;
+    const int64_t cb = row_code_bytes(fmt, rows);
+    int64_t c;
+#pragma omp parallel for schedule(static)
+    for (c = 0; c < cols; ++c) {
+        int64_t b;
+        for (b = 0; b < nb; ++b) {
+            float blockv[MXO_BLOCK];
+            uint8_t blk[MXO_BLOCK];
+            uint8_t s;
+            int i;
+            for (i = 0; i < MXO_BLOCK; ++i) blockv[i] = x[(b * MXO_BLOCK + i) * cols + c];
+            quantize_block(blockv, fmt, blk, &s);
+            store_codes(fmt, blk, b * MXO_BLOCK, codes + c * cb);
+            scales[c * nb + b] = s;
+        }
+    }
+    return 0;
+}
+
+/* Round a binary32 value to the nearest bfloat16 (8 significant bits, the
+ * binary32 exponent range), ties to even -- the IEEE conversion; NaN stays NaN
+ * (quiet).  Returns the bfloat16 bit pattern. */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if (isnan(f)) return (uint16_t)((u >> 16) | 0x0040u);
+    const uint32_t keep = u >> 16;          /* truncated result */
+    const uint32_t rest = u & 0xFFFFu;       /* dropped 16 bits */
+    uint32_t r = keep;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u; /* carry may reach Inf: correct */
+    return (uint16_t)r;
+}
+
+/* dequantize_block with a bfloat16 result: the exact value (as in
+ * mxo_dequantize: element * 2^(byte-127), 0xFF -> NaN) rounded once to the
+ * nearest bfloat16, ties to even.  The value fits binary32 exactly (at most 4
+ * significant bits, exponent within binary32's range or beyond its largest
+ * finite value, where binary32 and bfloat16 both give infinity), so rounding
+ * the binary32 value is rounding the exact one. */
+int mxo_dequantize_bf16(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                        int fmt, uint16_t* y)
+{
+    int rc = check_shape(fmt, rows, cols);
+    if (rc) return rc;
+    const int64_t nb = cols / MXO_BLOCK;
+    const int64_t cb = row_code_bytes(fmt, cols);
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t k;
+        for (k = 0; k < cols; ++k) {
+            int s = scales[r * nb + k / MXO_BLOCK];
+            double v = mxo_decode_element(fmt, load_code(fmt, codes + r * cb, k)) * mxo_decode_scale(s);
+            y[r * cols + k] = f32_to_bf16_rne((float)v);
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * block_matmul as the pages' first version states it ([Dialect] "The four
+ * ops": the left operand an MX tensor, the right one plain f32): 
+ *   C[m,n] <- C0[m,n] + sum_k deqA[m,k] * B[k,n]
+ * with B row-major [K, N].  Each product is exact in binary64 (at most 4
+ * significant bits times a binary32 value); the sum is formed in binary64 in
+ * k order.  sabs is sum_k |deqA * B|, the scale of the parity tolerance.
+ * ------------------------------------------------------------------------- */
+int mxo_block_matmul_f32b(const uint8_t* a_codes, const uint8_t* a_scales, int a_fmt,
+                          const float* B, int64_t M, int64_t N, int64_t K, const float* C0,
+                          double* ref, double* sabs)
+{
+    if (check_shape(a_fmt, M, K) || N < 0) return 1;
+    const int64_t nb = K / MXO_BLOCK;
+    const int64_t cb = row_code_bytes(a_fmt, K);
+    int64_t m;
+#pragma omp parallel for schedule(static)
+    for (m = 0; m < M; ++m) {
+        int64_t n;
+        for (n = 0; n < N; ++n) {
+            double acc = (double)C0[m * N + n], s = 0.0;
+            int64_t k;
+            for (k = 0; k < K; ++k) {
+                double p = deq_exact(a_fmt, a_codes + m * cb, a_scales + m * nb, k) * (double)B[k * N + n];
+                acc += p;
+                s += fabs(p);
+            }
+            ref[m * N + n] = acc;
+            sabs[m * N + n] = s;
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * fold_scale ([Dialect] "The four ops": multiply an MX tensor by a scalar):
+ * for a scalar 2^j the product is the same codes with every scale byte
+ * increased by j, since an E8M0 byte is the exponent of a power of two
+ * ([Layout] "The E8M0 shared scale").  The byte saturates at 0 (2^-127) and
+ * 254 (2^127) -- the nearest representable scales -- and 0xFF (NaN) stays
+ * 0xFF.  A scalar that is not a positive power of two is not foldable.
+ * ------------------------------------------------------------------------- */
+void mxo_fold_scale(uint8_t* scales, int64_t count, int j)
+{
+    int64_t i;
+    for (i = 0; i < count; ++i) {
+        int b = scales[i];
+        if (b == 0xFF) continue;
+        b += j;
+        if (b < 0) b = 0;
+        if (b > 254) b = 254;
+        scales[i] = (uint8_t)b;
+    }
+}
+
+/* The exponent j of a foldable scalar (a positive finite power of two,
+ * subnormal ones included), or -1000 when the scalar is not foldable. */
+int mxo_fold_exponent(double scalar)
+{
+    if (!(scalar > 0.0) || !isfinite(scalar)) return -1000;
+    int ex;
+    double f = frexp(scalar, &ex);
+    if (f != 0.5) return -1000;
+    return ex - 1;
 }
 
 int mxo_num_threads(void)

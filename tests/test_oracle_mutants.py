@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from oracle import build as obuild
+import test_oracle_next as nxt
 import test_oracle_pins as pins
 
 E2M1, E4M3 = oracle.E2M1, oracle.E4M3
@@ -25,7 +26,7 @@ MUTANTS = {
     "scale_bias_decode": ("return ldexp(1.0, byte - 127);", "return ldexp(1.0, byte - 126);"),
     "clip_low": ("if (e < -127) e = -127;", "if (e < -126) e = -126;"),
     "no_nan_scale": ("if (byte == 0xFF) return NAN;", "if (byte == 0x1FF) return NAN;"),
-    "floor_log2_off": ("return ex - 1;", "return ex;"),
+    "floor_log2_off": ("(void)frexp(v, &ex);\n    return ex - 1;", "(void)frexp(v, &ex);\n    return ex;"),
     "e4m3_subnormal": ("return ldexp((double)M, -9);", "return ldexp((double)M, -10);"),
     "zero_block_scale": ("*scale = 127;\n        return;", "*scale = 0;\n        return;"),
     "signed_amax": ("double a = fabs((double)x[i]);", "double a = (double)x[i];"),
@@ -55,6 +56,35 @@ PIN_CALLS = [
 ]
 
 
+# mistakes in the functions beyond the three core ops, against their own pins
+MUTANTS_NEXT = {
+    "axis0_gather_transposed": ("blockv[i] = x[(b * MXO_BLOCK + i) * cols + c];",
+                                "blockv[i] = x[c * rows + b * MXO_BLOCK + i];"),
+    "bf16_ties_away": ("if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u;",
+                       "if (rest >= 0x8000u) r = keep + 1u;"),
+    "bf16_truncates": ("if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u;",
+                       "if (rest > 0xFFFFu) r = keep + 1u;"),
+    "f32b_b_transposed": ("* (double)B[k * N + n];", "* (double)B[n * K + k];"),
+    "f32b_drops_c0": ("double acc = (double)C0[m * N + n], s = 0.0;", "double acc = 0.0, s = 0.0;"),
+    "fold_touches_nan": ("if (b == 0xFF) continue;", "if (b == 0x1FF) continue;"),
+    "fold_saturates_at_255": ("if (b > 254) b = 254;", "if (b > 255) b = 255;"),
+    "fold_wraps_low": ("if (b < 0) b = 0;", "if (b < 0) b += 256;"),
+    "fold_exponent_off": ("return ex - 1;\n}\n\nint mxo_num_threads", "return ex;\n}\n\nint mxo_num_threads"),
+}
+
+PIN_CALLS_NEXT = [
+    (nxt.test_axis0_is_quantize_of_the_transpose, {"fmt": E4M3, "rows": 64, "cols": 33}),
+    (nxt.test_axis0_literal_column, {}),
+    (nxt.test_dequantize_bf16_every_code_and_scale, {"fmt": E4M3}),
+    (nxt.test_dequantize_bf16_literals, {}),
+    (nxt.test_f32b_matches_numpy, {"fmt": E2M1, "M": 17, "N": 9, "K": 96}),
+    (nxt.test_f32b_equals_mx_product_when_b_is_representable, {}),
+    (nxt.test_fold_scale_multiplies_by_power_of_two, {"fmt": E4M3}),
+    (nxt.test_fold_scale_saturates_and_keeps_nan, {}),
+    (nxt.test_fold_exponent, {}),
+]
+
+
 @pytest.fixture(scope="module")
 def src_text():
     with open(obuild.SRC) as f:
@@ -73,6 +103,25 @@ def test_planted_mistake_is_caught(name, src_text, tmp_path):
     caught = []
     with oracle.use_library(str(lib)):
         for fn, kw in PIN_CALLS:
+            try:
+                fn(**kw)
+            except (AssertionError, ValueError):
+                caught.append(fn.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS_NEXT))
+def test_planted_mistake_in_next_functions_is_caught(name, src_text, tmp_path):
+    old, new = MUTANTS_NEXT[name]
+    assert src_text.count(old) == 1, f"mutation anchor for {name} not unique"
+    src = tmp_path / "mutant.c"
+    src.write_text(src_text.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run([obuild._cc(), "-std=c99", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+                    str(src), "-o", str(lib), "-lm"], check=True)
+    caught = []
+    with oracle.use_library(str(lib)):
+        for fn, kw in PIN_CALLS_NEXT:
             try:
                 fn(**kw)
             except (AssertionError, ValueError):
