@@ -57,6 +57,12 @@ def _load() -> ctypes.CDLL:
     L.mx_block_matmul.restype = i32
     L.mx_scales_relayout.argtypes = [vp, i32, i64, i64, vp, i32, vp]
     L.mx_scales_relayout.restype = i32
+    L.mx_quantize_axis.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, i32, vp]
+    L.mx_quantize_axis.restype = i32
+    L.mx_dequantize_bf16.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp, vp]
+    L.mx_dequantize_bf16.restype = i32
+    L.mx_fold_scale.argtypes = [vp, i64, i64, i32, ctypes.c_double, vp]
+    L.mx_fold_scale.restype = i32
     L.mx_device_status.argtypes = [vp]
     L.mx_device_status.restype = i32
     L.mx_selftest_wait_timeout.argtypes = [u64, vp]
@@ -167,6 +173,57 @@ def mx_block_matmul(a_codes: torch.Tensor, a_scales: torch.Tensor, a_fmt: int,
                                _dev_ptr(b_codes, "b_codes", cb), _dev_ptr(b_scales, "b_scales", sb), b_fmt,
                                scale_layout, block_size, scale_type, M, N, K,
                                _dev_ptr(C, "C", M * N * 4), _stream(stream)))
+
+
+def mx_quantize_axis(x: torch.Tensor, axis: int, fmt: int, codes: torch.Tensor, scales: torch.Tensor,
+                     scale_layout: int = SCALES_ROWMAJOR, stream=None, block_size: int = BLOCK,
+                     scale_type: int = SCALE_E8M0) -> None:
+    """quantize_block of a [rows, cols] tensor along `axis`; axis 0 writes the
+    layout of the [cols, rows] transpose (the N x K operand of mx_block_matmul)."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [rows, cols]")
+    rows, cols = x.shape
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(x.dtype)
+    if dt is None:
+        raise ValueError(f"x dtype {x.dtype} (f32 or bf16 only)")
+    if rows * cols == 0:
+        return
+    o_rows, o_cols = (cols, rows) if axis == 0 else (rows, cols)
+    cb, sb = mx_codes_bytes(fmt, o_rows, o_cols), mx_scales_bytes(scale_layout, o_rows, o_cols)
+    if cb < 0 or sb < 0 or axis not in (0, 1):
+        _check(lib.mx_quantize_axis(None, dt, rows, cols, axis, fmt, block_size, scale_type, None, None,
+                                    scale_layout, None))
+    _check(lib.mx_quantize_axis(_dev_ptr(x, "x", 0), dt, rows, cols, axis, fmt, block_size, scale_type,
+                                _dev_ptr(codes, "codes", cb), _dev_ptr(scales, "scales", sb), scale_layout,
+                                _stream(stream)))
+
+
+def mx_dequantize_bf16(codes: torch.Tensor, scales: torch.Tensor, rows: int, cols: int, fmt: int,
+                       y: torch.Tensor, scale_layout: int = SCALES_ROWMAJOR, stream=None, block_size: int = BLOCK,
+                       scale_type: int = SCALE_E8M0) -> None:
+    """dequantize_block to bfloat16: (codes, scales) -> y, a bf16 [rows, cols] tensor."""
+    if rows * cols == 0:
+        return
+    if y.dtype != torch.bfloat16:
+        raise ValueError("y must be bfloat16")
+    cb, sb = mx_codes_bytes(fmt, rows, cols), mx_scales_bytes(scale_layout, rows, cols)
+    if cb < 0 or sb < 0:
+        _check(lib.mx_dequantize_bf16(None, None, rows, cols, fmt, block_size, scale_type, scale_layout, None,
+                                      None))
+    _check(lib.mx_dequantize_bf16(_dev_ptr(codes, "codes", cb), _dev_ptr(scales, "scales", sb), rows, cols,
+                                  fmt, block_size, scale_type, scale_layout, _dev_ptr(y, "y", rows * cols * 2),
+                                  _stream(stream)))
+
+
+def mx_fold_scale(scales: torch.Tensor, rows: int, cols: int, scalar: float,
+                  scale_layout: int = SCALES_ROWMAJOR, stream=None) -> None:
+    """fold_scale: multiply the MX tensor with these scales by a power-of-two scalar, in place."""
+    sb = mx_scales_bytes(scale_layout, rows, cols)
+    if sb < 0 or rows * cols == 0:
+        _check(lib.mx_fold_scale(None, rows, cols, scale_layout, float(scalar), None))
+        return
+    _check(lib.mx_fold_scale(_dev_ptr(scales, "scales", sb), rows, cols, scale_layout, float(scalar),
+                             _stream(stream)))
 
 
 def mx_scales_relayout(src: torch.Tensor, src_layout: int, rows: int, cols: int, dst: torch.Tensor,

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -159,6 +160,76 @@ mx_status_t mx_dequantize(const void* codes, const uint8_t* scales, int64_t rows
     cudaError_t e = mx::launch_dequantize(codes, scales, rows, cols, fmt, scale_layout, y,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+    return ok();
+}
+
+mx_status_t mx_quantize_axis(const void* x, mx_dtype_t x_dtype, int64_t rows, int64_t cols, int axis,
+                             mx_format_t fmt, int block_size, mx_scale_type_t scale_type, void* codes,
+                             uint8_t* scales, mx_scale_layout_t scale_layout, void* stream) {
+    if (axis == 1)
+        return mx_quantize(x, x_dtype, rows, cols, fmt, block_size, scale_type, codes, scales, scale_layout, stream);
+    if (axis != 0) return fail(MX_ERR_UNSUPPORTED, "block axis %d (0 or 1)", axis);
+    mx_status_t s;
+    if ((s = check_common(block_size, scale_type)) != MX_OK) return s;
+    if (!valid_fmt(fmt)) return fail(MX_ERR_UNSUPPORTED, "element format %d", (int)fmt);
+    if (x_dtype != MX_F32 && x_dtype != MX_BF16) return fail(MX_ERR_UNSUPPORTED, "input dtype %d", (int)x_dtype);
+    if (!valid_layout(scale_layout)) return fail(MX_ERR_UNSUPPORTED, "scale layout %d", (int)scale_layout);
+    if ((s = check_shape(cols, rows)) != MX_OK) return s;  // blocks run along rows
+    if (rows == 0 || cols == 0) return ok();
+    if (!x || !codes || !scales) return fail(MX_ERR_NULL, "x, codes and scales must be non-NULL");
+    if (!aligned(x, 16) || !aligned(codes, 16))
+        return fail(MX_ERR_ALIGN, "x and codes must be 16-byte aligned");
+    if (!aligned(scales, scale_layout == MX_SCALES_MMA ? 16 : 4))
+        return fail(MX_ERR_ALIGN, "scales must be %d-byte aligned", scale_layout == MX_SCALES_MMA ? 16 : 4);
+    const int64_t xb = rows * cols * (x_dtype == MX_F32 ? 4 : 2);
+    const int64_t cb = mx_codes_bytes(fmt, cols, rows), sb = mx_scales_bytes(scale_layout, cols, rows);
+    if (overlaps(x, xb, codes, cb) || overlaps(x, xb, scales, sb) || overlaps(codes, cb, scales, sb))
+        return fail(MX_ERR_UNSUPPORTED, "input and outputs overlap");
+    if ((s = check_device()) != MX_OK) return s;
+    cudaError_t e = mx::launch_quantize_axis0(x, x_dtype, rows, cols, fmt, codes, scales, scale_layout,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "axis-0 quantize launch");
+    return ok();
+}
+
+mx_status_t mx_dequantize_bf16(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                               mx_format_t fmt, int block_size, mx_scale_type_t scale_type,
+                               mx_scale_layout_t scale_layout, void* y, void* stream) {
+    mx_status_t s;
+    if ((s = check_common(block_size, scale_type)) != MX_OK) return s;
+    if (!valid_fmt(fmt)) return fail(MX_ERR_UNSUPPORTED, "element format %d", (int)fmt);
+    if (!valid_layout(scale_layout)) return fail(MX_ERR_UNSUPPORTED, "scale layout %d", (int)scale_layout);
+    if ((s = check_shape(rows, cols)) != MX_OK) return s;
+    if (rows == 0 || cols == 0) return ok();
+    if (!codes || !scales || !y) return fail(MX_ERR_NULL, "codes, scales and y must be non-NULL");
+    if (!aligned(codes, 16) || !aligned(y, 16)) return fail(MX_ERR_ALIGN, "codes and y must be 16-byte aligned");
+    if (overlaps(y, rows * cols * 2, codes, mx_codes_bytes(fmt, rows, cols)) ||
+        overlaps(y, rows * cols * 2, scales, mx_scales_bytes(scale_layout, rows, cols)))
+        return fail(MX_ERR_UNSUPPORTED, "output overlaps an input");
+    if ((s = check_device()) != MX_OK) return s;
+    cudaError_t e = mx::launch_dequantize_bf16(codes, scales, rows, cols, fmt, scale_layout, y,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "bf16 dequantize launch");
+    return ok();
+}
+
+mx_status_t mx_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, mx_scale_layout_t scale_layout,
+                          double scalar, void* stream) {
+    if (!valid_layout(scale_layout)) return fail(MX_ERR_UNSUPPORTED, "scale layout %d", (int)scale_layout);
+    mx_status_t s;
+    if ((s = check_shape(rows, cols)) != MX_OK) return s;
+    // foldable: a positive finite power of two (frexp mantissa exactly 1/2)
+    int ex = 0;
+    if (!(scalar > 0.0) || !std::isfinite(scalar) || std::frexp(scalar, &ex) != 0.5)
+        return fail(MX_ERR_UNSUPPORTED, "scalar %g is not a positive power of two", scalar);
+    const int j = ex - 1;
+    if (rows == 0 || cols == 0) return ok();
+    if (!scales) return fail(MX_ERR_NULL, "scales must be non-NULL");
+    if ((s = check_device()) != MX_OK) return s;
+    // beyond +-254 every byte saturates the same way
+    const int jc = j > 255 ? 255 : (j < -255 ? -255 : j);
+    cudaError_t e = mx::launch_fold_scale(scales, rows, cols, scale_layout, jc, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fold_scale launch");
     return ok();
 }
 

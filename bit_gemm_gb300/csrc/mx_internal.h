@@ -25,6 +25,12 @@ cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t 
                               int layout, float* y, cudaStream_t stream);
 cudaError_t launch_relayout(const uint8_t* src, int src_layout, int64_t rows, int64_t cols, uint8_t* dst,
                             int dst_layout, cudaStream_t stream);
+cudaError_t launch_dequantize_bf16(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols, int fmt,
+                                   int layout, void* y, cudaStream_t stream);
+cudaError_t launch_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, int layout, int j, cudaStream_t stream);
+// x [rows][cols] blocked along rows; codes/scales in the layout of the [cols][rows] transpose.
+cudaError_t launch_quantize_axis0(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, void* codes,
+                                  uint8_t* scales, int layout, cudaStream_t stream);
 
 struct GemmArgs {
     const void* a_codes;

@@ -475,11 +475,12 @@ __device__ __forceinline__ float scale_value(uint32_t s) {
 // of contiguous f32 (one 256-bit store per lane when y is 32-byte aligned,
 // else two 128-bit stores) and one code load reads 256 (E4M3) or 128 (E2M1)
 // contiguous bytes.
-template <int FMT, int LAYOUT, bool kV8>
+template <int FMT, int LAYOUT, bool kV8, bool kBF16 = false>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const uint8_t* __restrict__ codes,
                                                                           const uint8_t* __restrict__ scales,
                                                                           int64_t nblocks, int64_t nb,
-                                                                          float* __restrict__ y) {
+                                                                          void* __restrict__ yv) {
+    float* __restrict__ y = static_cast<float*>(yv);
     const int lane = threadIdx.x & 31;
     const int64_t nwin = (nblocks + 7) / 8;
     const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
@@ -521,6 +522,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const 
                 const float mult = scale_value(sc[q]);
                 if (FMT == FMT_E2M1) decode8_e2m1(cw[q][0], mult, v);
                 else decode8_e4m3(cw[q][0], cw[q][1], mult, v);
+                if (kBF16) {
+                    // bfloat16 output: the exact value rounded to nearest, ties to
+                    // even (cvt.rn.bf16x2.f32); 16 bytes per lane, 512 per warp
+                    const __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+                    const __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+                    const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[4], v[5]);
+                    const __nv_bfloat162 p3 = __floats2bfloat162_rn(v[6], v[7]);
+                    uint4 o;
+                    o.x = *reinterpret_cast<const uint32_t*>(&p0);
+                    o.y = *reinterpret_cast<const uint32_t*>(&p1);
+                    o.z = *reinterpret_cast<const uint32_t*>(&p2);
+                    o.w = *reinterpret_cast<const uint32_t*>(&p3);
+                    __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(yv) + win * 256 + 8 * lane), o);
+                    continue;
+                }
                 float* dst = y + win * 256 + 8 * lane;
                 if (kV8) {
                     asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "f"(v[0]),
@@ -533,6 +549,146 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const 
             }
         }
     }
+}
+
+// ---------------------------------------------------------------- fold_scale
+//
+// Multiply an MX tensor by 2^j: every real scale byte b != 0xFF becomes
+// clamp(b + j, 0, 254); 0xFF (NaN) and the tensor-core layout's padding stay.
+__global__ void fold_scale_kernel(uint8_t* __restrict__ scales, int64_t rows, int64_t nb, int layout, int j) {
+    const int64_t total = rows * nb;
+    const int64_t nb4 = round_up(nb, 4);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        int64_t off = i;
+        if (layout == LAYOUT_MMA) {
+            const int64_t r = i / nb;
+            off = mma_scale_offset(r, i - r * nb, nb4);
+        }
+        const int b = scales[off];
+        if (b == 0xFF) continue;
+        int v = b + j;
+        v = v < 0 ? 0 : (v > 254 ? 254 : v);
+        scales[off] = (uint8_t)v;
+    }
+}
+
+// ---------------------------------------------------------- block axis 0
+//
+// Quantize x [rows][cols] in blocks of 32 consecutive ROWS of one column (the
+// reduction axis of a K x N right-hand operand) and write codes and scales in
+// the layout of the transposed tensor: codes [cols][rows] (packed as usual),
+// scales [cols][rows/32] (either layout, with cols as its rows).  A thread
+// owns kC adjacent columns and up to 4 consecutive blocks of them (128 rows);
+// a warp's loads of one input row are 32 * kC contiguous elements, and each
+// column's codes for its 4 blocks leave as contiguous 16- or 32-byte stores.
+// Rounding is the same as along the last axis: bf16 blocks go through
+// quantize_block_bf16, f32 blocks through quantize8.
+template <typename InT, int kC>
+struct Axis0Load;
+template <>
+struct Axis0Load<__nv_bfloat16, 2> {  // two columns per 32-bit load
+    static __device__ __forceinline__ void row(const __nv_bfloat16* p, uint32_t (&u)[2]) {
+        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(p));
+        u[0] = w << 16;
+        u[1] = w & 0xFFFF0000u;
+    }
+};
+template <>
+struct Axis0Load<__nv_bfloat16, 1> {
+    static __device__ __forceinline__ void row(const __nv_bfloat16* p, uint32_t (&u)[1]) {
+        u[0] = (uint32_t)__ldcs(reinterpret_cast<const unsigned short*>(p)) << 16;
+    }
+};
+template <>
+struct Axis0Load<float, 1> {
+    static __device__ __forceinline__ void row(const float* p, uint32_t (&u)[1]) {
+        u[0] = __float_as_uint(__ldcs(p));
+    }
+};
+
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_column_block(const uint32_t (&u)[32], bool bf16,
+                                                          uint32_t (&out)[FMT == FMT_E2M1 ? 4 : 8]) {
+    if (bf16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = (u[2 * i] >> 16) | (u[2 * i + 1] & 0xFFFF0000u);
+        return quantize_block_bf16<FMT>(w, out);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = max(m, u[i] & 0x7FFFFFFFu);
+    uint32_t sbyte = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t mn = 0xFFFFFFFFu;
+        uint32_t v[8], c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = u[8 * q + i];
+            mn = min(mn, v[i] & 0x7FFFFFFFu);
+        }
+        sbyte = quantize8<FMT>(v, m, mn, c);
+        if (FMT == FMT_E2M1) {
+            uint32_t wd = c[7];
+#pragma unroll
+            for (int i = 6; i >= 0; --i) wd = wd * 16u + c[i];
+            out[q] = wd;
+        } else {
+            out[2 * q] = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+            out[2 * q + 1] = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+        }
+    }
+    return sbyte;
+}
+
+template <typename InT, int kC, int FMT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads) quantize_axis0_kernel(const InT* __restrict__ x, int64_t rows,
+                                                                  int64_t cols, uint8_t* __restrict__ codes,
+                                                                  uint8_t* __restrict__ scales) {
+    constexpr int kCodeWords = FMT == FMT_E2M1 ? 4 : 8;
+    const int64_t nb = rows / 32;
+    const int64_t nb4 = round_up(nb, 4);
+    const int64_t ncg = (cols + kC - 1) / kC;  // column groups
+    const int64_t nrg = (nb + 3) / 4;           // groups of 4 blocks
+    const int64_t tasks = ncg * nrg;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t code_row = FMT == FMT_E2M1 ? rows / 2 : rows;  // bytes of one output row
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < tasks; t += stride) {
+        const int64_t cg = t % ncg, rg = t / ncg;
+        const int64_t c0 = cg * kC;
+        const int64_t b0 = rg * 4;
+        const int nblk = (int)min((int64_t)4, nb - b0);
+        for (int bi = 0; bi < nblk; ++bi) {
+            const int64_t r0 = (b0 + bi) * 32;
+            uint32_t u[kC][32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                uint32_t v[kC];
+                Axis0Load<InT, kC>::row(x + (r0 + i) * cols + c0, v);
+#pragma unroll
+                for (int c = 0; c < kC; ++c) u[c][i] = v[c];
+            }
+#pragma unroll
+            for (int c = 0; c < kC; ++c) {
+                const int64_t col = c0 + c;
+                if (col >= cols) break;
+                uint32_t out[kCodeWords];
+                const uint32_t sbyte = quantize_column_block<FMT>(u[c], sizeof(InT) == 2, out);
+                uint8_t* dst = codes + col * code_row + (FMT == FMT_E2M1 ? r0 / 2 : r0);
+                if (FMT == FMT_E2M1) {
+                    __stcs(reinterpret_cast<uint4*>(dst), make_uint4(out[0], out[1], out[2], out[3]));
+                } else {
+                    __stcs(reinterpret_cast<uint4*>(dst), make_uint4(out[0], out[1], out[2], out[3]));
+                    __stcs(reinterpret_cast<uint4*>(dst) + 1, make_uint4(out[4], out[5], out[6], out[7]));
+                }
+                const int64_t off = LAYOUT == LAYOUT_MMA ? mma_scale_offset(col, b0 + bi, nb4) : col * nb + b0 + bi;
+                scales[off] = (uint8_t)sbyte;
+            }
+        }
+    }
+    if (LAYOUT == LAYOUT_MMA) write_mma_padding(scales, cols, nb);
 }
 
 // ------------------------------------------------------------------ relayout
@@ -650,6 +806,70 @@ cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t 
     return deq_dispatch<false>(c, scales, nblocks, nb, fmt, layout, y, grid, st);
 }
 
+
+cudaError_t launch_dequantize_bf16(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols, int fmt,
+                                   int layout, void* y, cudaStream_t st) {
+    const int64_t nb = cols / 32;
+    const int64_t nblocks = rows * nb;
+    const int64_t nwin = (nblocks + 7) / 8;
+    const unsigned grid = (unsigned)grid_for((nwin * 32 + kUnroll - 1) / kUnroll, kMinBlocks);
+    const uint8_t* c = static_cast<const uint8_t*>(codes);
+    if (fmt == FMT_E2M1) {
+        if (layout == LAYOUT_MMA)
+            dequantize_kernel<FMT_E2M1, LAYOUT_MMA, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+        else
+            dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+    } else {
+        if (layout == LAYOUT_MMA)
+            dequantize_kernel<FMT_E4M3, LAYOUT_MMA, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+        else
+            dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, int layout, int j, cudaStream_t st) {
+    const int64_t nb = cols / 32;
+    if (rows * nb == 0) return cudaSuccess;
+    fold_scale_kernel<<<(unsigned)grid_for(rows * nb, 8), kThreads, 0, st>>>(scales, rows, nb, layout, j);
+    return cudaGetLastError();
+}
+
+namespace {
+template <typename InT, int kC, int FMT>
+cudaError_t axis0_layout(const InT* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales, int layout,
+                         cudaStream_t st) {
+    const int64_t nb = rows / 32;
+    const int64_t tasks = ((cols + kC - 1) / kC) * ((nb + 3) / 4);
+    int64_t grid = grid_for(tasks, 4);
+    if (layout == LAYOUT_MMA) {
+        const int64_t pad = (round_up(cols, 128) - cols) * round_up(nb, 4) + cols * (round_up(nb, 4) - nb);
+        const int64_t g2 = grid_for(pad, 4);
+        grid = grid > g2 ? grid : g2;
+        quantize_axis0_kernel<InT, kC, FMT, LAYOUT_MMA><<<(unsigned)grid, kThreads, 0, st>>>(x, rows, cols, codes, scales);
+    } else {
+        quantize_axis0_kernel<InT, kC, FMT, LAYOUT_ROWMAJOR><<<(unsigned)grid, kThreads, 0, st>>>(x, rows, cols, codes,
+                                                                                            scales);
+    }
+    return cudaGetLastError();
+}
+template <typename InT, int kC>
+cudaError_t axis0_fmt(const InT* x, int64_t rows, int64_t cols, int fmt, uint8_t* codes, uint8_t* scales, int layout,
+                      cudaStream_t st) {
+    return fmt == FMT_E2M1 ? axis0_layout<InT, kC, FMT_E2M1>(x, rows, cols, codes, scales, layout, st)
+                           : axis0_layout<InT, kC, FMT_E4M3>(x, rows, cols, codes, scales, layout, st);
+}
+}  // namespace
+
+cudaError_t launch_quantize_axis0(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, void* codes,
+                                  uint8_t* scales, int layout, cudaStream_t st) {
+    uint8_t* c = static_cast<uint8_t*>(codes);
+    if (dtype == DT_F32) return axis0_fmt<float, 1>(static_cast<const float*>(x), rows, cols, fmt, c, scales, layout, st);
+    const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(x);
+    // two columns per 32-bit load when every row starts on a 4-byte boundary
+    if ((cols & 1) == 0) return axis0_fmt<__nv_bfloat16, 2>(p, rows, cols, fmt, c, scales, layout, st);
+    return axis0_fmt<__nv_bfloat16, 1>(p, rows, cols, fmt, c, scales, layout, st);
+}
 
 cudaError_t launch_relayout(const uint8_t* src, int src_layout, int64_t rows, int64_t cols, uint8_t* dst,
                             int dst_layout, cudaStream_t st) {

@@ -153,6 +153,43 @@ MX_API mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales,
                             mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
                             float* C, void* stream);
 
+/* quantize_block along an explicit block axis ([Dialect] "The block axis":
+ * blocks run along the reduction axis, which for the right-hand operand of a
+ * product is its first axis).
+ *   axis = 1 : exactly mx_quantize (blocks of 32 along cols; cols % 32 == 0).
+ *   axis = 0 : blocks of 32 consecutive ROWS of one column (rows % 32 == 0,
+ *              cols any).  Outputs are laid out as the transposed tensor's
+ *              would be: codes mx_codes_bytes(fmt, cols, rows) bytes, row c
+ *              holding column c's codes; scales mx_scales_bytes(scale_layout,
+ *              cols, rows), with cols as the scale layout's rows.  The result
+ *              is directly the N x K operand B of mx_block_matmul for a K x N
+ *              input.  Codes and scales equal mx_quantize of the transpose.
+ * Other arguments, alignment and errors as mx_quantize; axis outside {0, 1}
+ * is MX_ERR_UNSUPPORTED. */
+MX_API mx_status_t mx_quantize_axis(const void* x, mx_dtype_t x_dtype, int64_t rows, int64_t cols, int axis,
+                             mx_format_t fmt, int block_size, mx_scale_type_t scale_type, void* codes,
+                             uint8_t* scales, mx_scale_layout_t scale_layout, void* stream);
+
+/* dequantize_block with a bfloat16 result ([Dialect] "The four ops").  Each
+ * element is the exact value of mx_dequantize rounded to the nearest bfloat16,
+ * ties to even; 0xFF scales and E4M3FN NaN codes give NaN.
+ *   y : out, rows x cols bfloat16 (2 bytes each), row-major, 16-B aligned.
+ * Other arguments and errors as mx_dequantize. */
+MX_API mx_status_t mx_dequantize_bf16(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                               mx_format_t fmt, int block_size, mx_scale_type_t scale_type,
+                               mx_scale_layout_t scale_layout, void* y, void* stream);
+
+/* fold_scale ([Dialect] "The four ops"): multiply the MX tensor whose scales
+ * these are (rows x cols elements) by `scalar`, in place, by adding j to every
+ * scale byte where scalar = 2^j ([Layout] "The E8M0 shared scale": the byte is
+ * the exponent of a power of two).  A byte saturates at 0 (2^-127) and 254
+ * (2^127); 0xFF stays NaN; the codes are untouched; the padding of
+ * MX_SCALES_MMA stays 0.  The result is exact wherever no byte saturates.
+ * A scalar that is not a positive finite power of two cannot be folded:
+ * MX_ERR_UNSUPPORTED, nothing launched. */
+MX_API mx_status_t mx_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, mx_scale_layout_t scale_layout,
+                          double scalar, void* stream);
+
 /* Re-lay scales between MX_SCALES_ROWMAJOR and MX_SCALES_MMA (both
  * directions; identical layouts copy).  src and dst must not overlap; sizes
  * as mx_scales_bytes().  The scale values are not changed. */

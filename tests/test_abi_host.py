@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 10
+    assert len(names) == 13
     out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (mx_\w+)", out))
     for n in names:
@@ -135,3 +135,49 @@ def test_python_binding_rejects_host_tensors():
     x = torch.zeros(4, 64)
     with pytest.raises((ValueError, RuntimeError, AssertionError)):
         mx.mx_quantize(x, mx.E2M1, torch.zeros(128, dtype=torch.uint8), torch.zeros(8, dtype=torch.uint8))
+
+
+def qa(x=A16, dt=mx.BF16, rows=64, cols=7, axis=0, fmt=mx.E4M3FN, bs=32, st=1, codes=A16 * 4, scales=A16 * 8,
+       layout=mx.SCALES_ROWMAJOR):
+    return L.mx_quantize_axis(x, dt, rows, cols, axis, fmt, bs, st, codes, scales, layout, None)
+
+
+def test_quantize_axis_validation():
+    assert qa(axis=2) == UNSUP and qa(axis=-1) == UNSUP
+    assert qa(rows=48) == SHAPE                 # axis 0 blocks run along rows
+    assert qa(axis=1, cols=7) == SHAPE          # axis 1 blocks run along cols
+    assert qa(bs=16) == UNSUP and qa(fmt=3) == UNSUP and qa(dt=9) == UNSUP
+    assert qa(x=None) == NULL and qa(scales=None) == NULL
+    assert qa(x=A16 + 4) == ALIGN
+    assert qa(codes=A16 + 64) == UNSUP          # overlaps x (64 x 7 bf16 = 896 B)
+    assert qa(rows=0) == OK and qa(cols=0) == OK
+    if not torch.cuda.is_available():
+        assert qa() == NODEV
+
+
+def fs(scales=A16, rows=8, cols=64, layout=mx.SCALES_ROWMAJOR, scalar=2.0):
+    return L.mx_fold_scale(scales, rows, cols, layout, scalar, None)
+
+
+def test_fold_scale_validation():
+    for bad in (3.0, -2.0, 0.0, -0.0, float("inf"), float("nan"), 1.5, 0.75):
+        assert fs(scalar=bad) == UNSUP, bad
+    assert fs(layout=5) == UNSUP
+    assert fs(rows=-1) == SHAPE and fs(cols=33) == SHAPE
+    assert fs(scales=None) == NULL
+    assert fs(rows=0) == OK
+    if not torch.cuda.is_available():
+        for good in (1.0, 0.5, 2.0 ** 100, 2.0 ** -1000):
+            assert fs(scalar=good) == NODEV, good
+
+
+def test_dequantize_bf16_validation():
+    d = lambda **k: L.mx_dequantize_bf16(k.get("codes", A16), k.get("scales", A16 * 4), k.get("rows", 4),
+                                         k.get("cols", 64), k.get("fmt", mx.E2M1), 32, 1,
+                                         k.get("layout", mx.SCALES_ROWMAJOR), k.get("y", A16 * 8), None)
+    assert d(cols=33) == SHAPE and d(fmt=3) == UNSUP and d(layout=5) == UNSUP
+    assert d(y=None) == NULL and d(y=A16 * 8 + 8) == ALIGN
+    assert d(y=A16 + 16) == UNSUP                # overlaps the codes
+    assert d(rows=0) == OK
+    if not torch.cuda.is_available():
+        assert d() == NODEV
