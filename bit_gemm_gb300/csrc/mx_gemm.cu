@@ -83,6 +83,7 @@ struct GemmParams {
     int32_t sf_rowmajor;   // 1: scales are row-major [rows][K/32]; gathered by the producer lanes
     int32_t nb;            // K / 32 (row stride of row-major scales, a multiple of 4)
     int32_t group_p;       // whole-tile order: bands of this many row tiles sweep all column tiles
+    int32_t op3d;          // 1: operand maps are 3-D [atoms][rows][128 B] (K a whole number of stages)
 };
 
 struct Work {
@@ -142,6 +143,7 @@ struct Cfg {
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int SFA_BYTES = G * 512;
     static constexpr int SFB_BYTES = G * SFB_TILES * 512;
+    static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);  // full scale boxes of a stage
     static constexpr int SF_COLS_A = 4 * G;
     static constexpr int SF_COLS_B = 4 * G * SFB_TILES;
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
@@ -232,6 +234,7 @@ __device__ __forceinline__ void epilogue_write_128(const GemmParams& p, const CU
 template <int KIND, int BN, int STAGES, int SWAP, int NBUF_>
 __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                 const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
     using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_>;
     constexpr int ACC = C_::ACC;
@@ -264,6 +267,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         fence_mbarrier_init();
         prefetch_tensormap(&tm_a);
         prefetch_tensormap(&tm_b);
+        if (!p.sf_rowmajor) {
+            prefetch_tensormap(&tm_sfa);
+            prefetch_tensormap(&tm_sfb);
+        }
         if (p.use_tma_epi) prefetch_tensormap(&tm_c);
     }
     if (warp == 1) {
@@ -282,6 +289,12 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         // tile layout (row r -> line r % 32, word (r / 32) % 4 of its tile).
         int stage = 0;
         uint32_t phase = 0;
+        const int li = lane & 3;
+        const void* lmap = li == 0 ? (const void*)&tm_a : li == 1 ? (const void*)&tm_b
+                                                    : li == 2 ? (const void*)&tm_sfa : (const void*)&tm_sfb;
+        const uint32_t lbase = smem_u32(smem) + (li == 0 ? C_::OFF_A : li == 1 ? C_::OFF_B
+                                                  : li == 2 ? C_::OFF_SFA : C_::OFF_SFB);
+        const uint32_t lstep = li == 0 ? C_::A_BYTES : li == 1 ? C_::B_BYTES : li == 2 ? C_::SFA_BYTES : C_::SFB_BYTES;
         uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
         uint32_t issued_phase = 0;
         bool ok = true;
@@ -306,23 +319,24 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                 // ragged K may need only the first)
                 const int g_first = kb * C_::G;
                 const int g_count = min(C_::G, p.sf_groups - g_first);
-                // scale row-tiles covering rows [q0, q0 + BN), clipped to the tensor
-                const int sfb_tiles = min(C_::SFB_TILES, (p.Q + 127) / 128 - (q0 >> 7));
-                if (lane == 0) {
-                    const uint32_t bytes = p.tx_a + p.tx_b +
-                                           (p.sf_rowmajor ? 0u : (uint32_t)(g_count * 512 + sfb_tiles * g_count * 512));
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    tma_load_2d(smem + C_::OFF_A + stage * C_::A_BYTES, &tm_a, kb * kRowBytes, p0, &full[stage]);
-                    tma_load_2d(smem + C_::OFF_B + stage * C_::B_BYTES, &tm_b, kb * kRowBytes, q0, &full[stage]);
-                    if (!p.sf_rowmajor) {
-                        const uint8_t* sa = p.sfa + ((int64_t)w.tp * p.sf_groups + g_first) * 512;
-                        bulk_load(smem + C_::OFF_SFA + stage * C_::SFA_BYTES, sa, g_count * 512, &full[stage]);
-                        for (int t = 0; t < sfb_tiles; ++t) {
-                            const uint8_t* sb = p.sfb + ((int64_t)((q0 >> 7) + t) * p.sf_groups + g_first) * 512;
-                            bulk_load(smem + C_::OFF_SFB + stage * C_::SFB_BYTES + t * C_::G * 512, sb,
-                                      g_count * 512, &full[stage]);
-                        }
+                // A stage is A, B and (tensor-core scale layout) the scale boxes
+                // of both, issued by lanes 0..3 with one instruction where the
+                // operand maps are 3-D; boxes past the tensor's end read zeros
+                // and count their full bytes.
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[stage], p.tx_a + p.tx_b + (p.sf_rowmajor ? 0u : C_::SF_TX));
+                {
+                    const int nl = p.sf_rowmajor ? 2 : 4;
+                    const uint32_t dst = lbase + (uint32_t)stage * lstep;
+                    const int32_t y = li == 0 ? p0 : li == 1 ? q0 : 4 * C_::G * kb;
+                    const int32_t z = li < 2 ? kb : (li == 2 ? w.tp : q0 >> 7);
+                    if (p.op3d) {
+                        if (lane < nl) tma_load_3d_at(dst, lmap, 0, y, z, &full[stage]);
+                    } else {
+                        if (lane < 2) tma_load_2d_at(dst, lmap, kb * kRowBytes, y, &full[stage]);
+                        else if (lane < nl) tma_load_3d_at(dst, lmap, 0, y, z, &full[stage]);
                     }
+                    __syncwarp();
                 }
                 if (p.sf_rowmajor) {
                     for (int g = 0; g < g_count; ++g) {
@@ -720,44 +734,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint32_t full_even = mapa_shared(smem_u32(full), 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            Work w;
-            for (int it = 0; ok && get_work(p, pair, npairs, it, w); ++it) {
-                const int32_t a_row = w.tp * 256 + (int32_t)rank * 128;
-                const int32_t b_row = w.tq * 256 + (int32_t)rank * 128;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err)) {
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    // the even CTA announces both CTAs' bytes; a load of the odd CTA
-                    // that lands first only takes the count below zero meanwhile
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.tx_a + p.tx_b + C_::SF_TX));
-                    const uint32_t bar = full_even + (uint32_t)stage * 8;
-                    tma_load_2d_pair(smem + C_::OFF_A + stage * C_::A_BYTES, &tm_a, kb * kRowBytes, a_row, bar);
-                    tma_load_2d_pair(smem + C_::OFF_B + stage * C_::B_BYTES, &tm_b, kb * kRowBytes, b_row, bar);
-                    tma_load_3d_pair(smem + C_::OFF_SFA + stage * C_::SFA_BYTES, &tm_sfa, 0, 4 * C_::G * kb,
-                                     a_row >> 7, bar);
-                    tma_load_3d_pair(smem + C_::OFF_SFB + stage * C_::SFB_BYTES, &tm_sfb, 0, 4 * C_::G * kb,
-                                     w.tq * 2, bar);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
+        // A stage is four loads -- A, B, A's scales, B's scales -- issued by
+        // lanes 0..3 with one instruction (3-D operand maps) or two.
+        const uint32_t full_even = mapa_shared(smem_u32(full), 0);
+        const int li = lane & 3;
+        const void* lmap = li == 0 ? (const void*)&tm_a : li == 1 ? (const void*)&tm_b
+                                                    : li == 2 ? (const void*)&tm_sfa : (const void*)&tm_sfb;
+        const uint32_t lbase = smem_u32(smem) + (li == 0 ? C_::OFF_A : li == 1 ? C_::OFF_B
+                                                  : li == 2 ? C_::OFF_SFA : C_::OFF_SFB);
+        const uint32_t lstep = li == 0 ? C_::A_BYTES : li == 1 ? C_::B_BYTES : li == 2 ? C_::SFA_BYTES : C_::SFB_BYTES;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        Work w;
+        for (int it = 0; ok && get_work(p, pair, npairs, it, w); ++it) {
+            const int32_t a_row = w.tp * 256 + (int32_t)rank * 128;
+            const int32_t b_row = w.tq * 256 + (int32_t)rank * 128;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
+                okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                if (!okw) {
+                    if (lane == 0) *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                // the even CTA announces both CTAs' bytes; a load of the odd CTA
+                // that lands first only takes the count below zero meanwhile
+                if (lane == 0 && rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.tx_a + p.tx_b + C_::SF_TX));
+                const uint32_t bar = full_even + (uint32_t)stage * 8;
+                const uint32_t dst = lbase + (uint32_t)stage * lstep;
+                // coordinates: operands (0, row, stage) in 3-D, (128 B * stage, row) in 2-D;
+                // scales (0, 4 G stage, 128-row tile)
+                const int32_t y = li == 0 ? a_row : li == 1 ? b_row : 4 * C_::G * kb;
+                const int32_t z = li < 2 ? kb : (li == 2 ? a_row >> 7 : w.tq * 2);
+                if (p.op3d) {
+                    if (lane < 4) tma_load_3d_pair_at(dst, lmap, 0, y, z, bar);
+                } else {
+                    if (lane < 2) tma_load_2d_pair_at(dst, lmap, kb * kRowBytes, y, bar);
+                    else if (lane < 4) tma_load_3d_pair_at(dst, lmap, 0, y, z, bar);
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
                 }
             }
-            if (!ok) {
-                // loads already issued count on the even CTA's barriers, which
-                // this CTA cannot wait on: give them time to land before the
-                // CTA may leave
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 100000) {
-                }
+        }
+        if (!ok && lane == 0) {
+            // loads already issued count on the even CTA's barriers, which
+            // this CTA cannot wait on: give them time to land before the
+            // CTA may leave
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 100000) {
             }
         }
         __syncwarp();
@@ -979,6 +1008,43 @@ bool make_operand_map(CUtensorMap* m, const void* codes, int64_t rows, int64_t K
     return r == CUDA_SUCCESS;
 }
 
+// The same codes viewed in 3-D as [stages][rows][one stage of K]: one stage of
+// a row is a 128-byte swizzle atom (128 E4M3 codes, 256 packed E2M1 codes, or
+// 128 E2M1 codes expanded to a byte each), the atom stride is its packed size
+// and the row stride a row's bytes, so the box {atom, box_rows, 1} at
+// (0, row, stage) is the 2-D box at (128 B * stage, row).  Only for K a whole
+// number of stages: a partial last atom would read into the next row.
+bool make_operand_map3(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int fmt_kind, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    cuuint64_t dims[3], strides[2];
+    if (fmt_kind == 0) {  // E4M3, one byte each
+        dims[0] = kRowBytes;
+        dims[2] = (cuuint64_t)(K / kRowBytes);
+        strides[0] = (cuuint64_t)K;
+        strides[1] = kRowBytes;
+    } else if (fmt_kind == 1) {  // packed E2M1 as bytes: an atom is 256 elements
+        dims[0] = kRowBytes;
+        dims[2] = (cuuint64_t)(K / (2 * kRowBytes));
+        strides[0] = (cuuint64_t)(K / 2);
+        strides[1] = kRowBytes;
+    } else {  // packed E2M1 expanded to a byte each in shared memory: an atom is 128 elements, 64 B in HBM
+        dt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+        dims[0] = kRowBytes;  // counted in 4-bit elements
+        dims[2] = (cuuint64_t)(K / kRowBytes);
+        strides[0] = (cuuint64_t)(K / 2);
+        strides[1] = kRowBytes / 2;
+    }
+    dims[1] = (cuuint64_t)rows;
+    cuuint32_t box[3] = {(cuuint32_t)kRowBytes, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, dt, 3, const_cast<void*>(codes), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Tensor map over C (rows x cols f32, row-major) for the reduce-add epilogue.
 bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_cols, int box_rows, int swizzle) {
     EncodeTiledFn enc = encode_fn();
@@ -1029,8 +1095,8 @@ bool make_sf_map(CUtensorMap* m, const uint8_t* sf, int64_t rows, int32_t sf_gro
 }
 
 template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0>
-cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p, int grid,
-                cudaStream_t st) {
+cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
+                const CUtensorMap& tc, const GemmParams& p, int grid, cudaStream_t st) {
     using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_>;
     auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_>;
     static int configured_for = -1;  // per-instantiation attribute (process-wide; one value for all devices)
@@ -1039,7 +1105,7 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
         if (e != cudaSuccess) return e;
         configured_for = C_::SMEM;
     }
-    kern<<<grid, C_::THREADS, C_::SMEM, st>>>(ta, tb, tc, p);
+    kern<<<grid, C_::THREADS, C_::SMEM, st>>>(ta, tb, tsa, tsb, tc, p);
     return cudaGetLastError();
 }
 
@@ -1142,7 +1208,9 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     p.nb = (int32_t)(a.K / 32);
     CUtensorMap ta, tb, tsa, tsb, tc;
     std::memset(&tc, 0, sizeof(tc));
-    if (!make_operand_map(&ta, x_codes, P, a.K, fk(x_fmt), 128) || !make_operand_map(&tb, y_codes, Q, a.K, fk(y_fmt), 128) ||
+    p.op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
+    auto opmap = p.op3d ? make_operand_map3 : make_operand_map;
+    if (!opmap(&ta, x_codes, P, a.K, fk(x_fmt), 128) || !opmap(&tb, y_codes, Q, a.K, fk(y_fmt), 128) ||
         !make_sf_map(&tsa, x_sf, P, p.sf_groups, g, 1) || !make_sf_map(&tsb, y_sf, Q, p.sf_groups, g, 2) ||
         (p.use_tma_epi && !make_c_map(&tc, a.C, a.M, a.N, 16, 32, 64))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
@@ -1194,9 +1262,16 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     }
 
     auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
-    CUtensorMap ta, tb, tc;
-    if (!make_operand_map(&ta, x_codes, P, a.K, fk(x_fmt), kBlockM) ||
-        !make_operand_map(&tb, y_codes, Q, a.K, fk(y_fmt), bn)) {
+    CUtensorMap ta, tb, tsa, tsb, tc;
+    const int op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
+    auto opmap = op3d ? make_operand_map3 : make_operand_map;
+    const int32_t sf_groups = (int32_t)(round_up(a.K / 32, 4) / 4);
+    const int gsz = kind == KIND_F4 ? 2 : 1;
+    std::memset(&tsa, 0, sizeof(tsa));
+    std::memset(&tsb, 0, sizeof(tsb));
+    if (!opmap(&ta, x_codes, P, a.K, fk(x_fmt), kBlockM) || !opmap(&tb, y_codes, Q, a.K, fk(y_fmt), bn) ||
+        (a.scale_layout == LAYOUT_MMA &&
+         (!make_sf_map(&tsa, x_sf, P, sf_groups, gsz, 1) || !make_sf_map(&tsb, y_sf, Q, sf_groups, gsz, (bn + 127) / 128)))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
         return cudaErrorInvalidValue;
     }
@@ -1236,6 +1311,7 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     p.tx_b = (uint32_t)bn * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
     p.sf_rowmajor = a.scale_layout == LAYOUT_ROWMAJOR ? 1 : 0;
     p.nb = (int32_t)(a.K / 32);
+    p.op3d = op3d;
     const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
     p.total_units = tiles * p.k_stages;
     p.group_p = band_rows(p.tiles_p, kBlockM * (x_fmt == FMT_E2M1 ? a.K / 2 : a.K));
@@ -1249,16 +1325,16 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
         grid = (int)(p.total_units < sms ? p.total_units : sms);
     }
 
-#define MX_RUN(KIND_, BN_, ST_, SW_) return run<KIND_, BN_, ST_, SW_>(ta, tb, tc, p, grid, st)
+#define MX_RUN(KIND_, BN_, ST_, SW_) return run<KIND_, BN_, ST_, SW_>(ta, tb, tsa, tsb, tc, p, grid, st)
     if (swap) {
         if (kind == KIND_F4) {
-            if (bn == 16) MX_RUN(KIND_F4, 16, 8, 1);
+            if (bn == 16) MX_RUN(KIND_F4, 16, 10, 1);
             if (bn == 32) MX_RUN(KIND_F4, 32, 8, 1);
             if (bn == 48) MX_RUN(KIND_F4, 48, 6, 1);
             MX_RUN(KIND_F4, 64, 6, 1);
         } else {
-            if (bn == 16) MX_RUN(KIND_F8F6F4, 16, 8, 1);
-            if (bn == 32) MX_RUN(KIND_F8F6F4, 32, 8, 1);
+            if (bn == 16) MX_RUN(KIND_F8F6F4, 16, 11, 1);
+            if (bn == 32) MX_RUN(KIND_F8F6F4, 32, 9, 1);
             if (bn == 48) MX_RUN(KIND_F8F6F4, 48, 6, 1);
             MX_RUN(KIND_F8F6F4, 64, 6, 1);
         }
