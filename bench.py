@@ -354,11 +354,21 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0):
         s = sets[i]
         mx.mx_block_matmul(s["ac"], s["as"], fa, s["bc"], s["bs"], fb, M, N, K, s["C"], L)
 
+    def fused(i):
+        # activations quantized inside the GEMM (one launch; M <= 64 only)
+        s = sets[i]
+        mx.mx_block_matmul_act(s["A"], fa, s["bc"], s["bs"], fb, N, s["C"])
+
     step(0)
     mx.mx_device_status()
+    sec_f = None
     with ClockSampler(dev_index) as clk:
         sec = max_over_ranks(timed_graph_steps(step, nsets, steps, warmup, world), world)
         sec_g = max_over_ranks(timed_graph_steps(gemm_only, nsets, steps, 3, world), world)
+        if quant_a and M <= 64:
+            fused(0)
+            mx.mx_device_status()
+            sec_f = max_over_ranks(timed_graph_steps(fused, nsets, steps, 3, world), world)
     mx.mx_device_status()
     flops = 2.0 * M * N * K
     tf_step = job_throughput(flops * steps, world, sec) / 1e12
@@ -373,6 +383,14 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0):
         "tensor_peak_tflops": peak_tf, "tensor_frac": tf_gemm / peak_tf,
         "gemm_gbs": gbs_gemm, "hbm_frac": gbs_gemm / peaks["hbm_gbs"], "gemm_bytes": gemm_bytes,
         "launches_per_step": 2 if quant_a else 1, "nsets": nsets, "clocks": clk.summary()}
+    if sec_f is not None:
+        # one launch: activations in (f32/bf16), weight codes and scales, C read and written
+        fused_bytes = a_bytes_in + mx.mx_codes_bytes(fb, N, K) + mx.mx_scales_bytes(L, N, K) + 8 * M * N
+        out["fused"] = {"step": "block_matmul_act (activations quantized in the GEMM)",
+                        "us_per_step": sec_f / steps * 1e6, "tflops": flops * steps / sec_f / 1e12,
+                        "gbs": fused_bytes * steps / sec_f / 1e9,
+                        "hbm_frac": fused_bytes * steps / sec_f / 1e9 / peaks["hbm_gbs"], "bytes": fused_bytes,
+                        "launches_per_step": 1}
     del sets, A, C0, bc, bs
     torch.cuda.empty_cache()
     return out

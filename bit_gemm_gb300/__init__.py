@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
     L.mx_dequantize_bf16.restype = i32
     L.mx_fold_scale.argtypes = [vp, i64, i64, i32, ctypes.c_double, vp]
     L.mx_fold_scale.restype = i32
+    L.mx_block_matmul_act.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, i64, i64, i64, vp, vp]
+    L.mx_block_matmul_act.restype = i32
     L.mx_device_status.argtypes = [vp]
     L.mx_device_status.restype = i32
     L.mx_selftest_wait_timeout.argtypes = [u64, vp]
@@ -224,6 +226,32 @@ def mx_fold_scale(scales: torch.Tensor, rows: int, cols: int, scalar: float,
         return
     _check(lib.mx_fold_scale(_dev_ptr(scales, "scales", sb), rows, cols, scale_layout, float(scalar),
                              _stream(stream)))
+
+
+def mx_block_matmul_act(a: torch.Tensor, a_fmt: int, b_codes: torch.Tensor, b_scales: torch.Tensor, b_fmt: int,
+                        N: int, C: torch.Tensor, stream=None, block_size: int = BLOCK,
+                        scale_type: int = SCALE_E8M0) -> None:
+    """C += quantize(a) * B with a f32/bf16 [M, K] quantized inside the GEMM (M <= 64); B given as [N, K]
+    codes with MX_SCALES_MMA scales; C f32 [M, N] in place."""
+    if a.dim() != 2:
+        raise ValueError("a must be 2-D [M, K]")
+    M, K = a.shape
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(a.dtype)
+    if dt is None:
+        raise ValueError(f"a dtype {a.dtype} (f32 or bf16 only)")
+    if M * N * K == 0:
+        _check(lib.mx_block_matmul_act(None, dt, a_fmt, None, None, b_fmt, SCALES_MMA, block_size, scale_type,
+                                       M, N, K, None, None))
+        return
+    if C.dtype != torch.float32:
+        raise ValueError("C must be float32")
+    cb, sb = mx_codes_bytes(b_fmt, N, K), mx_scales_bytes(SCALES_MMA, N, K)
+    if cb < 0 or sb < 0:
+        _check(lib.mx_block_matmul_act(None, dt, a_fmt, None, None, b_fmt, SCALES_MMA, block_size, scale_type,
+                                       M, N, K, None, None))
+    _check(lib.mx_block_matmul_act(_dev_ptr(a, "a", 0), dt, a_fmt, _dev_ptr(b_codes, "b_codes", cb),
+                                   _dev_ptr(b_scales, "b_scales", sb), b_fmt, SCALES_MMA, block_size, scale_type,
+                                   M, N, K, _dev_ptr(C, "C", M * N * 4), _stream(stream)))
 
 
 def mx_scales_relayout(src: torch.Tensor, src_layout: int, rows: int, cols: int, dst: torch.Tensor,

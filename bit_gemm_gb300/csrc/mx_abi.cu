@@ -233,6 +233,46 @@ mx_status_t mx_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, mx_scale_
     return ok();
 }
 
+mx_status_t mx_block_matmul_act(const void* a, mx_dtype_t a_dtype, mx_format_t a_fmt, const void* b_codes,
+                                const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t b_scale_layout,
+                                int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,
+                                void* stream) {
+    mx_status_t s;
+    if ((s = check_common(block_size, scale_type)) != MX_OK) return s;
+    if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt)) return fail(MX_ERR_UNSUPPORTED, "element formats %d, %d",
+                                                            (int)a_fmt, (int)b_fmt);
+    if (a_dtype != MX_F32 && a_dtype != MX_BF16) return fail(MX_ERR_UNSUPPORTED, "activation dtype %d", (int)a_dtype);
+    if (a_fmt == MX_E2M1 && b_fmt == MX_E4M3FN)
+        return fail(MX_ERR_UNSUPPORTED, "E2M1 activations need E2M1 weights here (quantize with mx_quantize instead)");
+    if (b_scale_layout != MX_SCALES_MMA)
+        return fail(MX_ERR_UNSUPPORTED, "the weights' scales must be in MX_SCALES_MMA");
+    if (M < 0 || N < 0 || K < 0) return fail(MX_ERR_SHAPE, "negative dimension");
+    if (M > 64)
+        return fail(MX_ERR_UNSUPPORTED,
+                    "M = %lld > 64: quantize A once with mx_quantize and use mx_block_matmul (a larger A would be "
+                    "quantized again for every column tile)", (long long)M);
+    if (K % 32) return fail(MX_ERR_SHAPE, "K %lld is not a multiple of the block size 32", (long long)K);
+    if (N > (1ll << 31) - 256 || K > (1ll << 31) - 256) return fail(MX_ERR_SHAPE, "dimension too large");
+    const bool mixed = a_fmt != b_fmt;
+    if (mixed && K % 128)
+        return fail(MX_ERR_SHAPE, "mixed E2M1/E4M3FN operands need K %% 128 == 0 (K = %lld)", (long long)K);
+    if (M == 0 || N == 0 || K == 0) return ok();
+    if (!a || !b_codes || !b_scales || !C) return fail(MX_ERR_NULL, "operand pointers must be non-NULL");
+    if (!aligned(a, 32)) return fail(MX_ERR_ALIGN, "the activations must be 32-byte aligned");
+    if (!aligned(b_codes, mixed ? 32 : 16) || !aligned(b_scales, 16) || !aligned(C, 16))
+        return fail(MX_ERR_ALIGN, "weight codes (32 B when E2M1 in a mixed product), scales and C must be 16-byte aligned");
+    const int64_t cb = M * N * 4;
+    if (overlaps(C, cb, a, M * K * (a_dtype == MX_F32 ? 4 : 2)) || overlaps(C, cb, b_codes, mx_codes_bytes(b_fmt, N, K)) ||
+        overlaps(C, cb, b_scales, mx_scales_bytes(MX_SCALES_MMA, N, K)))
+        return fail(MX_ERR_UNSUPPORTED, "C overlaps an input");
+    if ((s = check_device()) != MX_OK) return s;
+    mx::GemmActArgs g{a, a_dtype, a_fmt, b_codes, b_scales, b_fmt, M, N, K, C};
+    const char* detail = nullptr;
+    cudaError_t e = mx::launch_block_matmul_act(g, static_cast<cudaStream_t>(stream), &detail);
+    if (e != cudaSuccess) return detail ? fail(MX_ERR_CUDA, "%s", detail) : cuda_fail(e, "block_matmul_act launch");
+    return ok();
+}
+
 mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
                             const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
                             int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,

@@ -34,6 +34,7 @@
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
+#include "mx_quant_block.cuh"
 
 namespace mx {
 
@@ -84,6 +85,11 @@ struct GemmParams {
     int32_t nb;            // K / 32 (row stride of row-major scales, a multiple of 4)
     int32_t group_p;       // whole-tile order: bands of this many row tiles sweep all column tiles
     int32_t op3d;          // 1: operand maps are 3-D [atoms][rows][128 B] (K a whole number of stages)
+    int32_t k_atom0;       // first stage of K this launch covers (K split into launches)
+    // activations quantized in the kernel (MMA B operand, swapped shapes):
+    const void* act;       // [Q][act_ld] f32 or bf16, row-major
+    int64_t act_ld;        // elements per activation row
+    int32_t act_bf16;      // 1: bf16, 0: f32
 };
 
 struct Work {
@@ -125,8 +131,11 @@ __device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint3
     return true;
 }
 
-template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0>
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0>
 struct Cfg {
+    // ACT_ATOMS > 0: the activations (the MMA B operand of a swapped shape) are
+    // quantized by the kernel into a resident region of that many K stages
+    static constexpr bool ACT = ACT_ATOMS > 0;
     static constexpr int G = KIND == KIND_F4 ? 2 : 1;                 // scale groups per stage
     // 128-row scale tiles covering the BN rows of a B tile (tiles start on
     // 128-row boundaries: scale-factor TMEM addresses must stay aligned)
@@ -140,10 +149,12 @@ struct Cfg {
     static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
     static constexpr int THREADS = 32 * (GATE_WARP + 1);
     static constexpr int A_BYTES = kBlockM * kRowBytes;               // 16 KB
-    static constexpr int B_BYTES = BN * kRowBytes;
+    static constexpr int B_BYTES = ACT ? 0 : BN * kRowBytes;
     static constexpr int SFA_BYTES = G * 512;
-    static constexpr int SFB_BYTES = G * SFB_TILES * 512;
+    static constexpr int SFB_BYTES = ACT ? 0 : G * SFB_TILES * 512;
     static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);  // full scale boxes of a stage
+    static constexpr int ACT_BYTES = BN * kRowBytes;  // one resident K stage of the activations
+    static constexpr int ACT_SF_BYTES = G * 512;
     static constexpr int SF_COLS_A = 4 * G;
     static constexpr int SF_COLS_B = 4 * G * SFB_TILES;
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
@@ -162,10 +173,14 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_ACT = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_ACT_SF = OFF_ACT + ACT_ATOMS * ACT_BYTES;
+    static constexpr int OFF_EPI = (OFF_ACT_SF + ACT_ATOMS * ACT_SF_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * NBUF * EPI_BUF;
     static constexpr int BAR_BYTES = (2 * STAGES + 2 * ACC + 1) * 8 + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;           // + alignment slack
+    static_assert(!ACT || (SWAP && ACT_BYTES % 1024 == 0), "resident activations: swapped shapes, whole swizzle atoms");
+    static_assert(STAGES <= (ACT ? 14 : 15), "named barriers 1..STAGES (and 15 for the activation prologue)");
     static_assert(SF_SLOTS >= 2, "at least two scale slots in TMEM");
     static_assert(SF_COL0 + SF_SLOTS * SF_COLS_STAGE <= (int)kTmemCols, "TMEM columns");
     static_assert(ACC * BN <= SF_COL0, "accumulator columns");
@@ -231,12 +246,12 @@ __device__ __forceinline__ void epilogue_write_128(const GemmParams& p, const CU
     }
 }
 
-template <int KIND, int BN, int STAGES, int SWAP, int NBUF_>
-__global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1)
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_, int ACT_ATOMS = 0>
+__global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                 const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_>;
+    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
     constexpr int ACC = C_::ACC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -266,10 +281,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_a);
-        prefetch_tensormap(&tm_b);
+        if (!C_::ACT) prefetch_tensormap(&tm_b);  // resident activations: no B map
         if (!p.sf_rowmajor) {
             prefetch_tensormap(&tm_sfa);
-            prefetch_tensormap(&tm_sfb);
+            if (!C_::ACT) prefetch_tensormap(&tm_sfb);
         }
         if (p.use_tma_epi) prefetch_tensormap(&tm_c);
     }
@@ -282,6 +297,126 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // K stages this CTA touches (the hull of its work units), for the
+    // resident activations
+    int kb_lo = 0x7FFFFFFF, kb_hi = 0;
+    if constexpr (C_::ACT) {
+        Work w;
+        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+            kb_lo = min(kb_lo, w.kb0);
+            kb_hi = max(kb_hi, w.kb1);
+        }
+        if (kb_hi <= kb_lo) kb_lo = kb_hi = 0;
+        if (warp >= 1 && warp <= C_::GATE_WARP) {
+            // ------------------------------------------------ activation prologue
+            // The warps that are idle while the producer starts streaming the
+            // weights quantize this CTA's K stages of the activations once, with
+            // mx_quantize's rounding, into the MMA operand layout: per stage, BN
+            // rows of 128 bytes with the 128-byte swizzle, and the scale tile(s).
+            // Rows past M and elements past K become zero codes.
+            constexpr int BPA = KIND == KIND_F4 ? 8 : 4;  // 32-element blocks per stage
+            constexpr int AFMT = KIND == KIND_F4 ? FMT_E2M1 : FMT_E4M3;
+            const int nthr = 32 * C_::GATE_WARP;
+            const int64_t items = (int64_t)(kb_hi - kb_lo) * BN * BPA;
+            // block i: stage a, row r, block j of the stage; its first element k
+            auto item = [&](int64_t i, int& a, int& r, int& j, int64_t& k) {
+                j = (int)(i % BPA);
+                r = (int)((i / BPA) % BN);
+                a = (int)(i / (BPA * BN));
+                k = ((int64_t)(p.k_atom0 + kb_lo + a) * BPA + j) * 32;
+            };
+            auto emit = [&](const uint32_t (&u)[32], bool bf16, int a, int r, int j) {
+                uint32_t out[AFMT == FMT_E2M1 ? 4 : 8];
+                const uint32_t sbyte = quantize_column_block<AFMT>(u, bf16, out);
+                uint8_t* rowp = smem + C_::OFF_ACT + a * C_::ACT_BYTES + r * kRowBytes;
+                if constexpr (AFMT == FMT_E4M3) {  // a block is 32 bytes: chunks 2j, 2j+1
+                    *reinterpret_cast<uint4*>(rowp + (((2 * j) ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+                    *reinterpret_cast<uint4*>(rowp + (((2 * j + 1) ^ (r & 7)) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
+                } else {  // packed E2M1: a block is 16 bytes, chunk j
+                    *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+                }
+                smem[C_::OFF_ACT_SF + (a * C_::G + j / 4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3)] =
+                    (uint8_t)sbyte;
+            };
+            // loads are issued a batch at a time before any of them is used, so
+            // their latencies overlap
+            if (p.act_bf16) {
+                constexpr int kB = 4;
+                const __nv_bfloat16* act = static_cast<const __nv_bfloat16*>(p.act);
+                for (int64_t i0 = threadIdx.x - 32; i0 < items; i0 += (int64_t)nthr * kB) {
+                    uint32_t w16[kB][16];
+#pragma unroll
+                    for (int q = 0; q < kB; ++q) {
+                        int a, r, j;
+                        int64_t k;
+                        const int64_t i = i0 + (int64_t)q * nthr;
+                        item(i, a, r, j, k);
+                        if (i < items && r < p.Q && k < p.K) {
+                            load_block_bf16(act + (int64_t)r * p.act_ld + k, w16[q]);
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) w16[q][t] = 0;
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kB; ++q) {
+                        int a, r, j;
+                        int64_t k;
+                        const int64_t i = i0 + (int64_t)q * nthr;
+                        if (i >= items) break;
+                        item(i, a, r, j, k);
+                        uint32_t u[32];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            u[2 * t] = w16[q][t] << 16;
+                            u[2 * t + 1] = w16[q][t] & 0xFFFF0000u;
+                        }
+                        emit(u, true, a, r, j);
+                    }
+                }
+            } else {
+                constexpr int kB = 2;
+                const float* act = static_cast<const float*>(p.act);
+                for (int64_t i0 = threadIdx.x - 32; i0 < items; i0 += (int64_t)nthr * kB) {
+                    uint32_t u[kB][32];
+#pragma unroll
+                    for (int q = 0; q < kB; ++q) {
+                        int a, r, j;
+                        int64_t k;
+                        const int64_t i = i0 + (int64_t)q * nthr;
+                        item(i, a, r, j, k);
+                        if (i < items && r < p.Q && k < p.K) {
+                            const uint4* src = reinterpret_cast<const uint4*>(act + (int64_t)r * p.act_ld + k);
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                const uint4 v = __ldcs(src + t);
+                                u[q][4 * t] = v.x;
+                                u[q][4 * t + 1] = v.y;
+                                u[q][4 * t + 2] = v.z;
+                                u[q][4 * t + 3] = v.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) u[q][t] = 0;
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kB; ++q) {
+                        int a, r, j;
+                        int64_t k;
+                        const int64_t i = i0 + (int64_t)q * nthr;
+                        if (i >= items) break;
+                        item(i, a, r, j, k);
+                        emit(u[q], false, a, r, j);
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // generic writes, read by the tensor core
+            __syncwarp();
+            named_bar_sync(15, 32 * C_::GATE_WARP);
+        }
+    }
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // Lane 0 issues the TMA loads; with row-major scales every lane also
@@ -289,7 +424,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         // tile layout (row r -> line r % 32, word (r / 32) % 4 of its tile).
         int stage = 0;
         uint32_t phase = 0;
-        const int li = lane & 3;
+        // load roles: 0 A, 1 B, 2 A's scales, 3 B's scales (resident activations: A and its scales only)
+        const int li = C_::ACT ? ((lane & 1) ? 2 : 0) : (lane & 3);
         const void* lmap = li == 0 ? (const void*)&tm_a : li == 1 ? (const void*)&tm_b
                                                     : li == 2 ? (const void*)&tm_sfa : (const void*)&tm_sfb;
         const uint32_t lbase = smem_u32(smem) + (li == 0 ? C_::OFF_A : li == 1 ? C_::OFF_B
@@ -317,24 +453,24 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                 }
                 // scale groups present for this stage (the last stage of a
                 // ragged K may need only the first)
-                const int g_first = kb * C_::G;
+                const int g_first = (kb + p.k_atom0) * C_::G;
                 const int g_count = min(C_::G, p.sf_groups - g_first);
                 // A stage is A, B and (tensor-core scale layout) the scale boxes
                 // of both, issued by lanes 0..3 with one instruction where the
                 // operand maps are 3-D; boxes past the tensor's end read zeros
                 // and count their full bytes.
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&full[stage], p.tx_a + p.tx_b + (p.sf_rowmajor ? 0u : C_::SF_TX));
+                    mbar_arrive_expect_tx(&full[stage], p.tx_a + (C_::ACT ? 0u : p.tx_b) +
+                                                            (p.sf_rowmajor ? 0u : C_::SF_TX));
                 {
-                    const int nl = p.sf_rowmajor ? 2 : 4;
+                    const int kbg = kb + p.k_atom0;  // stage of K in the whole tensor
+                    const int nl = (C_::ACT || p.sf_rowmajor) ? 2 : 4;
                     const uint32_t dst = lbase + (uint32_t)stage * lstep;
-                    const int32_t y = li == 0 ? p0 : li == 1 ? q0 : 4 * C_::G * kb;
-                    const int32_t z = li < 2 ? kb : (li == 2 ? w.tp : q0 >> 7);
-                    if (p.op3d) {
-                        if (lane < nl) tma_load_3d_at(dst, lmap, 0, y, z, &full[stage]);
-                    } else {
-                        if (lane < 2) tma_load_2d_at(dst, lmap, kb * kRowBytes, y, &full[stage]);
-                        else if (lane < nl) tma_load_3d_at(dst, lmap, 0, y, z, &full[stage]);
+                    const int32_t y = li == 0 ? p0 : li == 1 ? q0 : 4 * C_::G * kbg;
+                    const int32_t z = li < 2 ? kbg : (li == 2 ? w.tp : q0 >> 7);
+                    if (lane < nl) {
+                        if (p.op3d || li >= 2) tma_load_3d_at(dst, lmap, 0, y, z, &full[stage]);
+                        else tma_load_2d_at(dst, lmap, kbg * kRowBytes, y, &full[stage]);
                     }
                     __syncwarp();
                 }
@@ -386,9 +522,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
         // only in the start-address field, which is advanced by adds) and the
         // four instruction descriptors carrying the scale-factor ids.
         const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
-        const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
+        const uint64_t b_desc0 = smem_desc(smem_u32(smem + (C_::ACT ? C_::OFF_ACT : C_::OFF_B)), 0, 1024, 2);
         const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
-        const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFB), 0, 128, 0);
+        const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + (C_::ACT ? C_::OFF_ACT_SF : C_::OFF_SFB)), 0, 128, 0);
         uint32_t idesc[kMmaPerStage];
 #pragma unroll
         for (int i = 0; i < kMmaPerStage; ++i) {
@@ -424,12 +560,15 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_>::THREADS, 1
                     if (p.sf_rowmajor) fence_proxy_async_smem();
                     const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
                     const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
-                    const uint64_t b_desc = b_desc0 + stage * (C_::B_BYTES >> 4);
+                    // B and its scales: the stage's ring slot, or the resident stage kb
+                    const uint64_t b_desc = C_::ACT ? b_desc0 + (kb - kb_lo) * (C_::ACT_BYTES >> 4)
+                                                    : b_desc0 + stage * (C_::B_BYTES >> 4);
                     const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
-                    const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
-                    const int g_first = kb * C_::G;
+                    const uint64_t sfb_desc = C_::ACT ? sfb_desc0 + (kb - kb_lo) * (C_::ACT_SF_BYTES >> 4)
+                                                      : sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
+                    const int g_first = (kb + p.k_atom0) * C_::G;
                     // valid MMAs in this stage (ragged K): each consumes 32 bytes of K
-                    const int rem = p.K - kb * k_elem_per_stage;
+                    const int rem = p.K - (kb + p.k_atom0) * k_elem_per_stage;
                     if (rem >= k_elem_per_stage) {
                         // full stage: everything unrolled.
                         // scale tiles -> TMEM: SFA group g at sf_col + 4g;
@@ -1094,11 +1233,11 @@ bool make_sf_map(CUtensorMap* m, const uint8_t* sf, int64_t rows, int32_t sf_gro
     return r == CUDA_SUCCESS;
 }
 
-template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0>
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                 const CUtensorMap& tc, const GemmParams& p, int grid, cudaStream_t st) {
-    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_>;
-    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_>;
+    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
+    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
     static int configured_for = -1;  // per-instantiation attribute (process-wide; one value for all devices)
     if (configured_for != C_::SMEM) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM);
@@ -1346,6 +1485,89 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     if (bn == 128) MX_RUN(KIND_F8F6F4, 128, 4, 0);
     MX_RUN(KIND_F8F6F4, 256, 4, 0);
 #undef MX_RUN
+}
+
+// Activations quantized inside the GEMM (swapped shapes, M <= 64): the MMA A
+// operand is the weights (N rows), the MMA B operand the activations, which
+// each CTA quantizes once for the K stages it touches.  K is covered by as
+// many launches as the resident region needs (each adds its part into C).
+namespace {
+template <int KIND, int BN, int STAGES, int ATOMS>
+cudaError_t run_act_chunks(const GemmActArgs& a, const CUtensorMap& ta, const CUtensorMap& tsa, const CUtensorMap& tc,
+                           GemmParams p, int64_t total_stages, cudaStream_t st) {
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof(none));
+    const int sms = sm_count();
+    for (int64_t c0 = 0; c0 < total_stages; c0 += ATOMS) {
+        p.k_atom0 = (int32_t)c0;
+        p.k_stages = (int32_t)(total_stages - c0 < ATOMS ? total_stages - c0 : ATOMS);
+        const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
+        p.total_units = tiles * p.k_stages;
+        int grid;
+        if (tiles >= sms || p.k_stages < 4) {
+            p.mode = 0;
+            grid = (int)(tiles < sms ? tiles : sms);
+        } else {
+            p.mode = 1;
+            grid = (int)(p.total_units < sms ? p.total_units : sms);
+        }
+        cudaError_t e = run<KIND, BN, STAGES, 1, 0, ATOMS>(ta, none, tsa, none, tc, p, grid, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t st, const char** detail) {
+    *detail = nullptr;
+    const int kind = (a.act_fmt == FMT_E2M1 && a.w_fmt == FMT_E2M1) ? KIND_F4 : KIND_F8F6F4;
+    const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
+    const int bn = (int)round_up(a.M, 16);  // 16..64
+    auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.P = (int32_t)a.N;
+    p.Q = (int32_t)a.M;
+    p.K = (int32_t)a.K;
+    p.tiles_p = (int32_t)((a.N + kBlockM - 1) / kBlockM);
+    p.tiles_q = 1;
+    p.sf_groups = (int32_t)(round_up(a.K / 32, 4) / 4);
+    p.wait_limit_ns = wait_limit_ns();
+    p.idesc = make_idesc(kind, a.w_fmt, a.act_fmt, bn);
+    p.swap = 1;
+    p.use_tma_epi = (a.N % 4) == 0 ? 1 : 0;
+    p.C = a.C;
+    p.ldc = a.N;
+    p.sfa = a.w_scales;
+    p.tx_a = (uint32_t)kBlockM * (fk(a.w_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.nb = (int32_t)(a.K / 32);
+    p.group_p = p.tiles_p;
+    p.op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
+    p.act = a.act;
+    p.act_ld = a.K;
+    p.act_bf16 = a.act_dtype == DT_BF16 ? 1 : 0;
+    CUtensorMap ta, tsa, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    auto opmap = p.op3d ? make_operand_map3 : make_operand_map;
+    if (!opmap(&ta, a.w_codes, a.N, a.K, fk(a.w_fmt), kBlockM) ||
+        !make_sf_map(&tsa, a.w_scales, a.N, p.sf_groups, kind == KIND_F4 ? 2 : 1, 1) ||
+        (p.use_tma_epi && !make_c_map(&tc, a.C, a.M, a.N, 32, bn, 0))) {
+        *detail = "cuTensorMapEncodeTiled rejected an operand";
+        return cudaErrorInvalidValue;
+    }
+    const int64_t total = (a.K + k_per_stage - 1) / k_per_stage;
+#define MX_ACT(KIND_, BN_, ST_, AT_) return run_act_chunks<KIND_, BN_, ST_, AT_>(a, ta, tsa, tc, p, total, st)
+    if (kind == KIND_F4) {
+        if (bn == 16) MX_ACT(KIND_F4, 16, 6, 32);
+        if (bn == 32) MX_ACT(KIND_F4, 32, 6, 16);
+        if (bn == 48) MX_ACT(KIND_F4, 48, 5, 12);
+        MX_ACT(KIND_F4, 64, 5, 8);
+    }
+    if (bn == 16) MX_ACT(KIND_F8F6F4, 16, 7, 32);
+    if (bn == 32) MX_ACT(KIND_F8F6F4, 32, 7, 16);
+    if (bn == 48) MX_ACT(KIND_F8F6F4, 48, 6, 12);
+    MX_ACT(KIND_F8F6F4, 64, 5, 8);
+#undef MX_ACT
 }
 
 }  // namespace mx

@@ -46,6 +46,19 @@ struct GemmArgs {
 // Returns cudaSuccess or an error; *detail gets a static explanation on failure.
 cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t stream, const char** detail);
 
+struct GemmActArgs {
+    const void* act;  // [M][K] f32 or bf16
+    int act_dtype;
+    int act_fmt;
+    const void* w_codes;  // [N][K], scales in the tensor-core layout
+    const uint8_t* w_scales;
+    int w_fmt;
+    int64_t M, N, K;
+    float* C;
+};
+// C += quantize(act) * W^T with the activations quantized inside the kernel (M <= 64).
+cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t stream, const char** detail);
+
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 // Limit (ns) for every bounded wait inside the library's kernels.

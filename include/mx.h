@@ -190,6 +190,25 @@ MX_API mx_status_t mx_dequantize_bf16(const void* codes, const uint8_t* scales, 
 MX_API mx_status_t mx_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, mx_scale_layout_t scale_layout,
                           double scalar, void* stream);
 
+/* block_matmul with the activations quantized on the fly ([Dialect] "The
+ * four ops": quantize_block then block_matmul, the step before the product
+ * folded into it): C <- C + quantize(a) * B, where `a` is M x K f32 or bf16
+ * (a_dtype), row-major, quantized to a_fmt along K exactly as mx_quantize
+ * would (same codes, same scales), inside the GEMM kernel -- the quantized
+ * activations never reach HBM.
+ *   B : N x K codes (b_fmt) with scales in MX_SCALES_MMA (b_scale_layout must
+ *       be MX_SCALES_MMA), as for mx_block_matmul.
+ *   C : M x N f32, read and written in place.
+ * For M <= 64 (decode-shaped products); a larger M returns MX_ERR_UNSUPPORTED
+ * (quantize A once with mx_quantize and call mx_block_matmul: a larger A would
+ * be quantized again for every column tile).  Formats: E4M3FN activations
+ * with E4M3FN or E2M1 weights, E2M1 activations with E2M1 weights.  `a` must
+ * be 32-B aligned; other rules, results and tolerance as mx_block_matmul. */
+MX_API mx_status_t mx_block_matmul_act(const void* a, mx_dtype_t a_dtype, mx_format_t a_fmt, const void* b_codes,
+                                const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t b_scale_layout,
+                                int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
+                                float* C, void* stream);
+
 /* Re-lay scales between MX_SCALES_ROWMAJOR and MX_SCALES_MMA (both
  * directions; identical layouts copy).  src and dst must not overlap; sizes
  * as mx_scales_bytes().  The scale values are not changed. */

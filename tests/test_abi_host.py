@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (mx_\w+)", out))
     for n in names:
@@ -181,3 +181,22 @@ def test_dequantize_bf16_validation():
     assert d(rows=0) == OK
     if not torch.cuda.is_available():
         assert d() == NODEV
+
+
+def ga(a=A16 * 2, dt=mx.BF16, fa=mx.E4M3FN, b=A16 * 64, sb=A16 * 128, fb=mx.E2M1, layout=mx.SCALES_MMA, bs=32, st=1,
+       M=16, N=256, K=256, C=A16 * 256):
+    return L.mx_block_matmul_act(a, dt, fa, b, sb, fb, layout, bs, st, M, N, K, C, None)
+
+
+def test_block_matmul_act_validation():
+    assert ga(M=65) == UNSUP                      # larger M: quantize once, then mx_block_matmul
+    assert ga(fa=mx.E2M1, fb=mx.E4M3FN) == UNSUP  # E2M1 activations with E4M3 weights
+    assert ga(layout=mx.SCALES_ROWMAJOR) == UNSUP
+    assert ga(dt=9) == UNSUP and ga(bs=16) == UNSUP
+    assert ga(K=96) == SHAPE                      # mixed formats need K % 128 == 0
+    assert ga(K=33) == SHAPE and ga(M=-1) == SHAPE
+    assert ga(a=None) == NULL and ga(C=None) == NULL
+    assert ga(a=A16 * 2 + 16) == ALIGN            # activations 32-byte aligned
+    assert ga(M=0) == OK
+    if not torch.cuda.is_available():
+        assert ga() == NODEV
