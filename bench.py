@@ -396,6 +396,90 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0):
     return out
 
 
+FFMA_PER_SM_CLK = 128  # f32 fused multiply-adds per SM per clock (4 partitions x 32 lanes)
+
+
+def bench_next(mx, steps, warmup, world, peaks, dev_index):
+    """The entry points beyond the three core ops, each on its own workload:
+    block_matmul with an f32 right operand (workload 6, decode-shaped; the
+    activations are quantized before timing), quantize along the first axis
+    and dequantize to bf16 (workload 2's tensor), and fold_scale (workload 2's
+    scales)."""
+    out = {}
+    # ---- block_matmul_f32b: C += deq(A) * B, B f32 K x N (235 MB > L2: no rotation needed)
+    w = workloads.make(6)
+    M, N, K = w["M"], w["N"], w["K"]
+    ac, as_ = mx.alloc_codes(M, K, mx.E4M3FN), mx.alloc_scales(M, K)
+    mx.mx_quantize(w["A"].cuda(), mx.E4M3FN, ac, as_)
+    B = torch.from_numpy(w["B"]).cuda()
+    C = torch.from_numpy(w["C0"]).cuda()
+    f_bytes = mx.mx_codes_bytes(mx.E4M3FN, M, K) + mx.mx_scales_bytes(mx.SCALES_ROWMAJOR, M, K) + 4 * K * N + 8 * M * N
+
+    def f32b(i):
+        mx.mx_block_matmul_f32b(ac, as_, mx.E4M3FN, B, M, C)
+
+    f32b(0)
+    mx.mx_device_status()
+    with ClockSampler(dev_index) as clk:
+        sec = max_over_ranks(timed_graph_steps(f32b, 1, steps, warmup, world), world)
+    mx.mx_device_status()
+    ck = clk.summary()
+    flops = 2.0 * M * N * K
+    gbs = f_bytes * steps / sec / 1e9
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = ck["sm_max_mhz"] or 2070.0
+    alu_peak = sms * FFMA_PER_SM_CLK * 2 * mhz * 1e6 / 1e12
+    out["block_matmul_f32b"] = {
+        "workload": workloads.NAMES[6], "M": M, "N": N, "K": K, "formats": "E4M3 x f32",
+        "us_per_step": sec / steps * 1e6, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"], "bytes": f_bytes,
+        "tflops": flops * steps / sec / 1e12, "ffma_peak_tflops": alu_peak,
+        "alu_frac": flops * steps / sec / 1e12 / alu_peak, "launches_per_step": 1, "clocks": ck}
+    del B, C, ac, as_, w
+    torch.cuda.empty_cache()
+
+    # ---- quantize along axis 0, dequantize to bf16, fold_scale: workload 2's tensor
+    w = workloads.make(2)
+    rows, cols = w["rows"], w["cols"]
+    n = rows * cols
+    qb = 2 * n + n + n // 32
+    db = n + n // 32 + 2 * n
+    fb = 2 * (n // 32)
+    x0 = w["x"].cuda()
+    nsets = sets_for(qb + db)
+    sets = [{"x": x0.clone(), "codes": mx.alloc_codes(rows, cols, mx.E4M3FN), "scales": mx.alloc_scales(rows, cols),
+             "y": torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")} for _ in range(nsets)]
+
+    def q_axis0(i):
+        s = sets[i]
+        mx.mx_quantize_axis(s["x"], 0, mx.E4M3FN, s["codes"], s["scales"])
+
+    def deq_bf16(i):
+        s = sets[i]
+        mx.mx_dequantize_bf16(s["codes"], s["scales"], rows, cols, mx.E4M3FN, s["y"])
+
+    def fold(i):
+        s = sets[i]
+        mx.mx_fold_scale(s["scales"], rows, cols, 2.0)
+
+    for i in range(nsets):
+        q_axis0(i)
+    mx.mx_device_status()
+    k = max(steps, 200)
+    sec_q = max_over_ranks(timed_graph_steps(q_axis0, nsets, k, 3, world), world)
+    sec_d = max_over_ranks(timed_graph_steps(deq_bf16, nsets, k, 3, world), world)
+    sec_f = max_over_ranks(timed_graph_steps(fold, nsets, k, 3, world), world)
+    mx.mx_device_status()
+    for name, b, sec_k, what in (("quantize_axis0", qb, sec_q, "bf16 4096x4096 -> MXFP8, blocks down the columns"),
+                                 ("dequantize_bf16", db, sec_d, "MXFP8 4096x4096 -> bf16"),
+                                 ("fold_scale", fb, sec_f, "scale bytes of a 4096x4096 MX tensor, times 2")):
+        g = b * k / sec_k / 1e9
+        out[name] = {"what": what, "us": sec_k / k * 1e6, "gbs": g, "hbm_frac": g / peaks["hbm_gbs"], "bytes": b,
+                     "nsets": nsets}
+    del sets, x0
+    torch.cuda.empty_cache()
+    return out
+
+
 def measured_traffic(key: str):
     """DRAM bytes per launch from the committed ncu capture, or None when the
     kernel source has changed since the counters were taken."""
@@ -486,7 +570,7 @@ def main():
     ap.add_argument("--gemm-steps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--only", choices=["headline", "decode", "square", "prefill"], default=None,
+    ap.add_argument("--only", choices=["headline", "decode", "square", "prefill", "next"], default=None,
                     help="run one workload only, print its numbers and exit (profiling runs)")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="row-count scale of the GEMM workloads with --only (1 = full size)")
@@ -509,6 +593,8 @@ def main():
         if args.only == "headline":
             hl = bench_headline(mx, args.steps, args.warmup, world, peaks, dev_index)
             out = {k: v for k, v in hl.items() if k not in ("x_host",)}
+        elif args.only == "next":
+            out = bench_next(mx, args.steps, args.warmup, world, peaks, dev_index)
         else:
             cfg = {"decode": 3, "square": 4, "prefill": 5}[args.only]
             out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale, dev_index)
@@ -521,6 +607,7 @@ def main():
     if not args.no_gemm:
         for cfg in (3, 4, 5):
             gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks, 1.0, dev_index))
+    nxt = None if args.no_gemm else bench_next(mx, args.gemm_steps, max(3, args.warmup), world, peaks, dev_index)
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(hl["x_host"])
@@ -542,6 +629,7 @@ def main():
                      "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"},
         "kernels": {"quantize": hl["quantize"], "dequantize": hl["dequantize"]},
         "block_matmul": gemms,
+        "next": nxt,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": hl["launches"],

@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
     L.mx_fold_scale.restype = i32
     L.mx_block_matmul_act.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, i64, i64, i64, vp, vp]
     L.mx_block_matmul_act.restype = i32
+    L.mx_block_matmul_f32b.argtypes = [vp, vp, i32, i32, i32, i32, vp, i64, i64, i64, vp, vp]
+    L.mx_block_matmul_f32b.restype = i32
     L.mx_device_status.argtypes = [vp]
     L.mx_device_status.restype = i32
     L.mx_selftest_wait_timeout.argtypes = [u64, vp]
@@ -252,6 +254,28 @@ def mx_block_matmul_act(a: torch.Tensor, a_fmt: int, b_codes: torch.Tensor, b_sc
     _check(lib.mx_block_matmul_act(_dev_ptr(a, "a", 0), dt, a_fmt, _dev_ptr(b_codes, "b_codes", cb),
                                    _dev_ptr(b_scales, "b_scales", sb), b_fmt, SCALES_MMA, block_size, scale_type,
                                    M, N, K, _dev_ptr(C, "C", M * N * 4), _stream(stream)))
+
+
+def mx_block_matmul_f32b(a_codes: torch.Tensor, a_scales: torch.Tensor, a_fmt: int, B: torch.Tensor, M: int,
+                         C: torch.Tensor, scale_layout: int = SCALES_ROWMAJOR, stream=None, block_size: int = BLOCK,
+                         scale_type: int = SCALE_E8M0) -> None:
+    """C += dequantize(A) * B with A [M, K] codes/scales and B f32 [K, N] row-major; C f32 [M, N] in place."""
+    if B.dim() != 2:
+        raise ValueError("B must be 2-D [K, N]")
+    K, N = B.shape
+    if M * N * K == 0:
+        _check(lib.mx_block_matmul_f32b(None, None, a_fmt, scale_layout, block_size, scale_type, None, M, N, K,
+                                        None, None))
+        return
+    if B.dtype != torch.float32 or C.dtype != torch.float32:
+        raise ValueError("B and C must be float32")
+    cb, sb = mx_codes_bytes(a_fmt, M, K), mx_scales_bytes(scale_layout, M, K)
+    if cb < 0 or sb < 0:
+        _check(lib.mx_block_matmul_f32b(None, None, a_fmt, scale_layout, block_size, scale_type, None, M, N, K,
+                                        None, None))
+    _check(lib.mx_block_matmul_f32b(_dev_ptr(a_codes, "a_codes", cb), _dev_ptr(a_scales, "a_scales", sb), a_fmt,
+                                    scale_layout, block_size, scale_type, _dev_ptr(B, "B", K * N * 4), M, N, K,
+                                    _dev_ptr(C, "C", M * N * 4), _stream(stream)))
 
 
 def mx_scales_relayout(src: torch.Tensor, src_layout: int, rows: int, cols: int, dst: torch.Tensor,

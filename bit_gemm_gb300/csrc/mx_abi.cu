@@ -273,6 +273,35 @@ mx_status_t mx_block_matmul_act(const void* a, mx_dtype_t a_dtype, mx_format_t a
     return ok();
 }
 
+mx_status_t mx_block_matmul_f32b(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt,
+                                 mx_scale_layout_t a_scale_layout, int block_size, mx_scale_type_t scale_type,
+                                 const float* B, int64_t M, int64_t N, int64_t K, float* C, void* stream) {
+    mx_status_t s;
+    if ((s = check_common(block_size, scale_type)) != MX_OK) return s;
+    if (!valid_fmt(a_fmt)) return fail(MX_ERR_UNSUPPORTED, "element format %d", (int)a_fmt);
+    if (!valid_layout(a_scale_layout)) return fail(MX_ERR_UNSUPPORTED, "scale layout %d", (int)a_scale_layout);
+    if (M < 0 || N < 0 || K < 0) return fail(MX_ERR_SHAPE, "negative dimension");
+    if (K % 32) return fail(MX_ERR_SHAPE, "K %lld is not a multiple of the block size 32", (long long)K);
+    if (M > (1ll << 40) || N > (1ll << 31) - 1024 || K > (1ll << 31) - 1024)
+        return fail(MX_ERR_SHAPE, "dimension too large");
+    if (M == 0 || N == 0 || K == 0) return ok();  // C += (empty sum) is C
+    if (N % 4) return fail(MX_ERR_ALIGN, "N %lld: rows of B and C must be whole 16-byte units (N %% 4 == 0)",
+                           (long long)N);
+    if (!a_codes || !a_scales || !B || !C) return fail(MX_ERR_NULL, "operand pointers must be non-NULL");
+    if (!aligned(a_codes, 16) || !aligned(a_scales, 16) || !aligned(B, 16) || !aligned(C, 16))
+        return fail(MX_ERR_ALIGN, "A codes, A scales, B and C must be 16-byte aligned");
+    const int64_t cb = M * N * 4;
+    if (overlaps(C, cb, a_codes, mx_codes_bytes(a_fmt, M, K)) ||
+        overlaps(C, cb, a_scales, mx_scales_bytes(a_scale_layout, M, K)) || overlaps(C, cb, B, K * N * 4))
+        return fail(MX_ERR_UNSUPPORTED, "C overlaps an input");
+    if ((s = check_device()) != MX_OK) return s;
+    mx::GemmF32bArgs g{a_codes, a_scales, a_fmt, a_scale_layout, B, M, N, K, C};
+    const char* detail = nullptr;
+    cudaError_t e = mx::launch_block_matmul_f32b(g, static_cast<cudaStream_t>(stream), &detail);
+    if (e != cudaSuccess) return detail ? fail(MX_ERR_CUDA, "%s", detail) : cuda_fail(e, "block_matmul_f32b launch");
+    return ok();
+}
+
 mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
                             const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
                             int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,

@@ -1118,6 +1118,38 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
+bool encode_tiled_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (uint32_t i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    return enc(m, dt, rank, const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned* device_error_word() {
+    static unsigned* word = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_mx_device_error) == cudaSuccess) word = static_cast<unsigned*>(p);
+        else cudaGetLastError();
+    });
+    return word;
+}
+
+namespace {
+
 // Tensor map over the codes of an operand with `rows` rows of K elements.
 // fmt_kind: 0 = one byte per element (E4M3), 1 = packed E2M1 as bytes,
 // 2 = packed E2M1 expanded to one byte per element in shared memory.

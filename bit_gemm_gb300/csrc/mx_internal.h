@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mx {
@@ -58,6 +59,27 @@ struct GemmActArgs {
 };
 // C += quantize(act) * W^T with the activations quantized inside the kernel (M <= 64).
 cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t stream, const char** detail);
+
+struct GemmF32bArgs {
+    const void* a_codes;  // [M][K] in a_fmt
+    const uint8_t* a_scales;
+    int a_fmt;
+    int a_layout;
+    const float* B;  // [K][N] row-major, N % 4 == 0
+    int64_t M, N, K;
+    float* C;
+};
+// C += dequantize(A) * B on the CUDA cores (B has no MX encoding).
+cudaError_t launch_block_matmul_f32b(const GemmF32bArgs& a, cudaStream_t stream, const char** detail);
+
+// The library's device error word (raised by bounded waits that give up).
+unsigned* device_error_word();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point; false if
+// the entry point is missing or the encoder rejects the arguments.
+bool encode_tiled_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 

@@ -190,6 +190,25 @@ MX_API mx_status_t mx_dequantize_bf16(const void* codes, const uint8_t* scales, 
 MX_API mx_status_t mx_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, mx_scale_layout_t scale_layout,
                           double scalar, void* stream);
 
+/* block_matmul with an unquantized right operand ([Dialect] "The four ops":
+ * the first form of block_matmul, an MX tensor times a plain f32 one):
+ *   C <- C + dequantize(A) * B
+ *   A : M x K codes (a_fmt) with scales in a_scale_layout, blocked along K.
+ *   B : K x N f32, row-major (not transposed, no scales).
+ *   C : M x N f32, row-major, read and written in place.
+ * Each output is the exact sum of C and the products deq(a)*b, up to f32
+ * rounding: partial sums are formed per 32-element block of A and per share
+ * of K, so |C - exact| stays within 1e-5 * sum |deq(a) * b|.  The order in
+ * which the shares of K are added into C is not fixed, so repeated calls may
+ * differ in the last bits.  A 0xFF scale poisons its block: every output
+ * that uses the block is NaN.
+ * N % 4 == 0 (rows of B and C start on 16-byte boundaries: MX_ERR_ALIGN
+ * otherwise); all four pointers 16-B aligned; K % 32 == 0; C must not
+ * overlap an input.  An empty product returns MX_OK without launching. */
+MX_API mx_status_t mx_block_matmul_f32b(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt,
+                                 mx_scale_layout_t a_scale_layout, int block_size, mx_scale_type_t scale_type,
+                                 const float* B, int64_t M, int64_t N, int64_t K, float* C, void* stream);
+
 /* block_matmul with the activations quantized on the fly ([Dialect] "The
  * four ops": quantize_block then block_matmul, the step before the product
  * folded into it): C <- C + quantize(a) * B, where `a` is M x K f32 or bf16

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (mx_\w+)", out))
     for n in names:
@@ -200,3 +200,20 @@ def test_block_matmul_act_validation():
     assert ga(M=0) == OK
     if not torch.cuda.is_available():
         assert ga() == NODEV
+
+
+def gf(a=A16, sa=A16 * 2, fa=mx.E4M3FN, layout=mx.SCALES_ROWMAJOR, bs=32, st=1, B=A16 * 64, M=16, N=256, K=256,
+       C=A16 * 256):
+    return L.mx_block_matmul_f32b(a, sa, fa, layout, bs, st, B, M, N, K, C, None)
+
+
+def test_block_matmul_f32b_validation():
+    assert gf(fa=3) == UNSUP and gf(layout=4) == UNSUP and gf(bs=16) == UNSUP
+    assert gf(K=33) == SHAPE and gf(N=-1) == SHAPE
+    assert gf(N=258) == ALIGN                     # rows of B and C on 16-byte boundaries
+    assert gf(B=None) == NULL and gf(C=None) == NULL
+    assert gf(B=A16 * 64 + 4) == ALIGN and gf(C=A16 * 256 + 8) == ALIGN
+    assert gf(C=A16 * 64) == UNSUP                # C overlaps B
+    assert gf(M=0) == OK and gf(K=0) == OK
+    if not torch.cuda.is_available():
+        assert gf() == NODEV

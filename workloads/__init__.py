@@ -20,6 +20,11 @@ CPU torch.bfloat16 tensor):
   4 ``square_mxfp8_8192``: A, Bt f32 8192x8192 N(0,1); C0 uniform[-1,1].
   5 ``prefill_mxfp4_8192x28672x8192``: A bf16 8192x8192 N(0,1) with 0.1% of
     positions multiplied by 100; W f32 28672x8192 N(0, 0.02); C0 zeros.
+  6 ``decode_f32b_16x14336x4096``: the product with an unquantized f32 right
+    operand: A bf16 16x4096 N(0,1) (quantized to MXFP8 before the product);
+    B f32 4096x14336 (K x N, row-major) N(0, 0.02) with one element per column
+    multiplied by 20 (the per-output-channel outliers of workload 3's W, drawn
+    directly in the K x N orientation); C0 f32 16x14336 N(0,1).
 
 ``scale`` (0 < scale <= 1) shrinks the row counts of the large workloads for
 quick runs; the full workloads use scale = 1.
@@ -35,6 +40,7 @@ NAMES = {
     3: "decode_mixed_16x14336x4096",
     4: "square_mxfp8_8192",
     5: "prefill_mxfp4_8192x28672x8192",
+    6: "decode_f32b_16x14336x4096",
 }
 
 BLOCK = 32
@@ -120,7 +126,18 @@ def workload5(seed: int = 0, scale: float = 1.0):
     return {"A": A, "W": W, "C0": C0, "M": M, "N": N, "K": K}
 
 
+def workload6(seed: int = 0, scale: float = 1.0):
+    rng = np.random.default_rng(seed)
+    M, N, K = 16, _rows(14336, scale) // 4 * 4, 4096
+    A = _bf16(_normal(rng, (M, K)))
+    B = _normal(rng, (K, N), 0.02)
+    rows = rng.integers(0, K, N)
+    B[rows, np.arange(N)] *= np.float32(20.0)
+    C0 = _normal(rng, (M, N))
+    return {"A": A, "B": B, "C0": C0, "M": M, "N": N, "K": K}
+
+
 def make(cfg: int, seed: int = 0, scale: float = 1.0):
     if cfg == 1:
         return workload1(seed)
-    return {2: workload2, 3: workload3, 4: workload4, 5: workload5}[cfg](seed, scale)
+    return {2: workload2, 3: workload3, 4: workload4, 5: workload5, 6: workload6}[cfg](seed, scale)
