@@ -19,19 +19,27 @@
 // 8 MB (K = 4096) column strip of B is re-read from L2, not HBM.
 //
 // Per CTA: warp 0 streams B by TMA, one K step (32 rows x 512 f32 = 64 KB,
-// two 256-column boxes) per stage through a ring of stages; warps 1..8
-// compute.  Each compute warp also decodes its share of A's block for the
-// step (16 rows x 32 codes, unscaled values) into shared memory, with the
-// scale kept aside: a thread sums the 32 products of a block in f32 first and
-// multiplies by the block's scale 2^(s-127) once (exact unless it leaves the
-// binary32 range), folding the block sum into its running sum with one FMA.
-// That keeps the f32 rounding error of an output near (32 + number of blocks)
-// units in the last place of sum |a*b| instead of K of them.
+// two 256-column boxes, issued by two lanes) per stage through a ring of
+// stages, and decodes A's block for the step (16 rows x 32 codes, unscaled
+// values, raw codes loaded two steps ahead) into the stage's slot; the stage
+// is full when both the bytes and the decoded block have arrived.  Warps
+// 1..8 compute and wait on nothing else, so they drift freely within the
+// ring.  The block's scale is kept aside: a thread sums the 32 products of a
+// block in f32 first and multiplies by the block's scale 2^(s-127) once
+// (exact unless it leaves the binary32 range), folding the block sum into its
+// running sum with one FMA.  That keeps the f32 rounding error of an output
+// near (32 + number of blocks) units in the last place of sum |a*b| instead
+// of K of them.
 //
 // Thread (warp w = 1..8, lane l): columns 4g..4g+3 of the tile with
 // g = 32*((w-1) % 4) + l, rows 8*((w-1) / 4) .. +7; 32 sums and 32 block sums
-// in registers.  Per K row it reads one float4 of B (a warp reads 512
-// contiguous bytes: no bank conflicts) and two broadcast float4 of A.
+// in registers, updated two rows at a time by packed f32x2 FMAs.  Per K row
+// it reads one float4 of B (a warp reads 512 contiguous bytes: no bank
+// conflicts) and two broadcast float4 of A.
+//
+// Measured on the decode shape (16 x 14336 x 4096, B 235 MB): the kernel
+// runs within about 10% of the same pipeline with the arithmetic removed,
+// i.e. it is bound by streaming B.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -44,23 +52,27 @@
 namespace mx {
 namespace {
 
-constexpr int kF_Rows = 16;                        // rows of C per tile
-constexpr int kF_Cols = 512;                       // columns of C per tile
-constexpr int kF_Half = 256;                       // columns per TMA box
-constexpr int kF_KStep = 32;                       // rows of B per stage (one MX block of A)
+constexpr int kF_Rows = 16;                                 // rows of C per tile
+constexpr int kF_Cols = 512;                                // columns of C per tile
+constexpr int kF_KStep = 32;                                // rows of B per stage (16: half an MX block)
 constexpr int kF_Stages = 3;
-constexpr int kF_RowGroups = 2;                    // compute warps split the 16 rows in two
-constexpr int kF_TM = kF_Rows / kF_RowGroups;      // rows per thread
-constexpr int kF_Workers = 4 * kF_RowGroups;       // compute warps
-constexpr int kF_Threads = 32 * (kF_Workers + 1);  // + the TMA warp
-constexpr int kF_HalfBytes = kF_KStep * kF_Half * 4;
-constexpr int kF_StageBytes = 2 * kF_HalfBytes;    // 64 KB
-constexpr int kF_OffA = kF_Stages * kF_StageBytes;               // decoded A: [2][32 k][16 rows] f32
-constexpr int kF_OffS = kF_OffA + 2 * kF_KStep * kF_Rows * 4;   // block scales: [2][16] f32
-constexpr int kF_OffBar = kF_OffS + 2 * kF_Rows * 4;
-constexpr int kF_Smem = kF_OffBar + 2 * kF_Stages * 8 + 1024;     // + alignment slack
-static_assert(kF_Rows * kF_KStep / 2 == 32 * kF_Workers, "one pair of A codes per compute thread");
-static_assert(kF_Smem <= 227 * 1024, "shared memory");
+constexpr int kF_CtasPerSm = 1;
+constexpr int kF_RowGroups = 2;                             // the 16 rows are split over this many threads
+constexpr int kF_Box = 256;                                 // columns per TMA box
+constexpr int kF_Boxes = kF_Cols / kF_Box;
+constexpr int kF_ColGroups = kF_Cols / 4;                   // a thread owns 4 columns
+constexpr int kF_TM = kF_Rows / kF_RowGroups;               // rows per thread
+constexpr int kF_Workers = kF_ColGroups * kF_RowGroups / 32;  // compute warps
+constexpr int kF_Threads = 32 * (kF_Workers + 1);           // + the TMA warp
+constexpr int kF_BoxBytes = kF_KStep * kF_Box * 4;
+constexpr int kF_StageBytes = kF_Boxes * kF_BoxBytes;
+constexpr int kF_OffA = kF_Stages * kF_StageBytes;                      // decoded A: [stage][k][16 rows] f32
+constexpr int kF_OffS = kF_OffA + kF_Stages * kF_KStep * kF_Rows * 4;  // block scales: [stage][16] f32
+constexpr int kF_OffBar = kF_OffS + kF_Stages * kF_Rows * 4;
+constexpr int kF_Smem = kF_OffBar + 2 * kF_Stages * 8 + 1024;          // + alignment slack
+static_assert(kF_Cols % kF_Box == 0 && kF_Boxes <= 32 && (kF_KStep == 16 || kF_KStep == 32), "tile shape");
+static_assert(kF_TM % 4 == 0, "rows per thread are read as float4");
+static_assert(kF_Smem * kF_CtasPerSm <= 227 * 1024, "shared memory");
 
 struct F32bParams {
     const uint8_t* a_codes;
@@ -69,8 +81,8 @@ struct F32bParams {
     int64_t a_row_bytes;  // bytes of codes per row of A
     int64_t nb, nb4;      // blocks per row; rounded up to 4 (tensor-core scale layout)
     int a_layout;
-    int MT, NT, KB;       // row tiles, column tiles, K steps
-    int64_t total;        // MT * NT * KB units
+    int MT, NT, KS;       // row tiles, column tiles, K steps
+    int64_t total;        // MT * NT * KS units
     float* C;
     uint64_t wait_limit_ns;
     unsigned* err;
@@ -96,11 +108,33 @@ __device__ __forceinline__ float block_scale(uint32_t s) {
     return s == 0xFFu ? __uint_as_float(0x7FC00000u) : (s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u));
 }
 
+// Packed pairs of f32 (low word = first): fma.rn.f32x2 / mul.rn.f32x2 do two
+// IEEE binary32 operations per instruction, each rounded as fmaf / a * b are,
+// which halves the instructions the compute warps issue.
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpk2(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 struct Unit {
-    int kb, mt, nt;
+    int ks, mt, nt;  // K step, row tile, column tile
     __device__ __forceinline__ void next(const F32bParams& p) {
-        if (++kb == p.KB) {
-            kb = 0;
+        if (++ks == p.KS) {
+            ks = 0;
             if (++mt == p.MT) {
                 mt = 0;
                 ++nt;
@@ -112,35 +146,70 @@ struct Unit {
 
 __device__ __forceinline__ Unit unit_at(const F32bParams& p, int64_t u) {
     Unit w;
-    w.kb = (int)(u % p.KB);
-    const int64_t t = u / p.KB;
+    w.ks = (int)(u % p.KS);
+    const int64_t t = u / p.KS;
     w.mt = (int)(t % p.MT);
     w.nt = (int)(t / p.MT);
     return w;
 }
 
-// The two codes and (for j == 0) the scale byte of row m of the tile, K step kb.
+// One lane's share of A for a K step: row (lane & 15) of the row tile, codes
+// h*KStep/2 .. (h+1)*KStep/2 - 1 of the step with h = lane >> 4 (one load of
+// 4 to 16 bytes), and the scale byte of the step's block (lanes 0..15).  Rows
+// past M read as zero codes.
+struct ARaw {
+    uint4 c;
+    uint32_t s;
+};
+
 template <int FMT>
-__device__ __forceinline__ void load_a_raw(const F32bParams& p, const Unit& w, int m, int j, uint32_t& codes,
-                                           uint32_t& sbyte) {
-    const int64_t row = (int64_t)w.mt * kF_Rows + m;
-    codes = 0;
-    sbyte = 127;
+__device__ __forceinline__ ARaw load_a_raw(const F32bParams& p, const Unit& w, int lane) {
+    constexpr int kBytes = (FMT == FMT_E4M3 ? kF_KStep : kF_KStep / 2) / 2;  // code bytes per lane
+    ARaw r{make_uint4(0, 0, 0, 0), 127};
+    const int64_t row = (int64_t)w.mt * kF_Rows + (lane & 15);
+    const int h = lane >> 4;
     if (row < p.M) {
-        const uint8_t* rp = p.a_codes + row * p.a_row_bytes;
-        if constexpr (FMT == FMT_E4M3) codes = __ldg(reinterpret_cast<const uint16_t*>(rp + (int64_t)w.kb * 32) + j);
-        else codes = __ldg(rp + (int64_t)w.kb * 16 + j);
-        if (j == 0)
-            sbyte = __ldg(p.a_scales + (p.a_layout == LAYOUT_MMA ? mma_scale_offset(row, w.kb, p.nb4)
-                                                                 : row * p.nb + w.kb));
+        const uint8_t* src = p.a_codes + row * p.a_row_bytes + ((int64_t)w.ks * 2 + h) * kBytes;
+        if constexpr (kBytes == 16) {
+            r.c = __ldg(reinterpret_cast<const uint4*>(src));
+        } else if constexpr (kBytes == 8) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+            r.c.x = v.x;
+            r.c.y = v.y;
+        } else {
+            r.c.x = __ldg(reinterpret_cast<const uint32_t*>(src));
+        }
+        if (h == 0) {
+            const int64_t kb = (int64_t)w.ks * kF_KStep / 32;
+            r.s = __ldg(p.a_scales + (p.a_layout == LAYOUT_MMA ? mma_scale_offset(row, kb, p.nb4) : row * p.nb + kb));
+        }
     }
+    return r;
+}
+
+// The lane's codes as exact values into dec[k][row] (k-major), and its scale.
+template <int FMT>
+__device__ __forceinline__ void store_a(const ARaw& r, int lane, float* dec, float* scl) {
+    const int row = lane & 15, k0 = (lane >> 4) * (kF_KStep / 2);
+    const uint32_t wv[4] = {r.c.x, r.c.y, r.c.z, r.c.w};
+#pragma unroll
+    for (int i = 0; i < kF_KStep / 4; ++i) {
+        // pair i: elements k0 + 2i, k0 + 2i + 1
+        const float2 v = FMT == FMT_E4M3 ? decode2_e4m3(wv[i >> 1] >> (16 * (i & 1)))
+                                         : decode2_e2m1(wv[i >> 2] >> (8 * (i & 3)));
+        dec[(k0 + 2 * i) * kF_Rows + row] = v.x;
+        dec[(k0 + 2 * i + 1) * kF_Rows + row] = v.y;
+    }
+    if (lane < 16) scl[row] = block_scale(r.s);
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kF_Threads, 1) gemm_f32b_kernel(const __grid_constant__ CUtensorMap tm_b,
+__global__ void __launch_bounds__(kF_Threads, kF_CtasPerSm) gemm_f32b_kernel(const __grid_constant__ CUtensorMap tm_b,
                                                                   const F32bParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by an offset from the array itself, so that the compiler keeps
+    // the accesses below as shared-memory loads and stores
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* a_dec = reinterpret_cast<float*>(smem + kF_OffA);
     float* a_scl = reinterpret_cast<float*>(smem + kF_OffS);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kF_OffBar);
@@ -152,7 +221,7 @@ __global__ void __launch_bounds__(kF_Threads, 1) gemm_f32b_kernel(const __grid_c
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_b);
         for (int s = 0; s < kF_Stages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);  // the TMA issue (with its bytes) and the decoded A
             mbar_init(&empty[s], kF_Workers);
         }
         fence_mbarrier_init();
@@ -161,25 +230,46 @@ __global__ void __launch_bounds__(kF_Threads, 1) gemm_f32b_kernel(const __grid_c
     if (u0 >= u1) return;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA
-        if (lane == 0) {
-            Unit w = unit_at(p, u0);
-            bool ok = true;
-            int64_t i = 0;
-            for (int64_t u = u0; u < u1; ++u, ++i, w.next(p)) {
-                const int stage = (int)(i % kF_Stages);
-                const uint32_t phase = (uint32_t)(i / kF_Stages) & 1u;
-                if (ok) ok = mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns, p.err);
-                if (!ok) break;  // the compute warps time out on `full` and skip the rest
-                const int32_t x = w.nt * kF_Cols, y = w.kb * kF_KStep;
-                const bool second = (int64_t)x + kF_Half < p.N;  // a box wholly past N is not loaded
-                uint8_t* dst = smem + stage * kF_StageBytes;
-                mbar_arrive_expect_tx(&full[stage], second ? kF_StageBytes : kF_HalfBytes);
-                tma_load_2d(dst, &tm_b, x, y, &full[stage]);
-                if (second) tma_load_2d(dst + kF_HalfBytes, &tm_b, x + kF_Half, y, &full[stage]);
+        // ------------------------------------------------ TMA and A decoding
+        // Per stage: lane 0 issues B's loads; then the warp decodes A's block
+        // into the stage's slot (raw codes loaded two steps ahead) and lane 0
+        // arrives a second time.
+        Unit w = unit_at(p, u0), w1 = w, w2 = w;
+        w1.next(p);
+        w2 = w1;
+        w2.next(p);
+        ARaw r0 = load_a_raw<FMT>(p, w, lane), r1{};
+        if (u0 + 1 < u1) r1 = load_a_raw<FMT>(p, w1, lane);
+        int64_t i = 0;
+        for (int64_t u = u0; u < u1; ++u, ++i) {
+            const int stage = (int)(i % kF_Stages);
+            const uint32_t phase = (uint32_t)(i / kF_Stages) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, p.wait_limit_ns, p.err);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;  // the compute warps time out on `full`
+            {
+                // lane b loads box b (columns x + 256b ..); boxes wholly past N are not loaded
+                const int32_t x = w.nt * kF_Cols, y = w.ks * kF_KStep;
+                const int64_t left = p.N - x;
+                const int nbox = left >= kF_Cols ? kF_Boxes : (int)((left + kF_Box - 1) / kF_Box);
+                if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(nbox * kF_BoxBytes));
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_2d(smem + stage * kF_StageBytes + lane * kF_BoxBytes, &tm_b, x + lane * kF_Box, y,
+                                &full[stage]);
             }
-            // every issued copy has landed before the CTA exits (normally long
-            // since: the compute warps waited for each of them)
+            store_a<FMT>(r0, lane, a_dec + stage * (kF_KStep * kF_Rows), a_scl + stage * kF_Rows);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[stage]);
+            r0 = r1;
+            if (u + 2 < u1) r1 = load_a_raw<FMT>(p, w2, lane);
+            w = w1;
+            w1 = w2;
+            w2.next(p);
+        }
+        // every issued copy has landed before the CTA exits (normally long
+        // since: the compute warps waited for each of them)
+        if (lane == 0) {
             const int64_t n = i;
             for (int64_t q = n > kF_Stages ? n - kF_Stages : 0; q < n; ++q)
                 if (!mbar_wait(&full[q % kF_Stages], (uint32_t)(q / kF_Stages) & 1u, p.wait_limit_ns, p.err)) break;
@@ -188,11 +278,10 @@ __global__ void __launch_bounds__(kF_Threads, 1) gemm_f32b_kernel(const __grid_c
     }
 
     // -------------------------------------------------------------- compute
-    const int t = threadIdx.x - 32;         // 0 .. 255
-    const int g = t & 127;                  // column group: columns 4g .. 4g+3 of the tile
-    const int rg = t >> 7;                  // row group: rows kF_TM*rg ..
-    const int am = t & 15, aj = t >> 4;     // this thread decodes codes 2aj, 2aj+1 of tile row am
-    const uint32_t b_off = (uint32_t)((g >> 6) * kF_HalfBytes + (g & 63) * 16);
+    const int t = threadIdx.x - 32;
+    const int g = t % kF_ColGroups;         // column group: columns 4g .. 4g+3 of the tile
+    const int rg = t / kF_ColGroups;        // row group: rows kF_TM*rg ..
+    const uint32_t b_off = (uint32_t)((g >> 6) * kF_BoxBytes + (g & 63) * 16);
 
     float acc[kF_TM][4];
 #pragma unroll
@@ -201,68 +290,61 @@ __global__ void __launch_bounds__(kF_Threads, 1) gemm_f32b_kernel(const __grid_c
         for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
 
     Unit w = unit_at(p, u0);
-    uint32_t raw_c, raw_s;
-    load_a_raw<FMT>(p, w, am, aj, raw_c, raw_s);
     bool live = true;  // false after a timed-out wait: the remaining units are skipped
     int64_t i = 0;
     for (int64_t u = u0; u < u1; ++u, ++i) {
-        const int buf = (int)(i & 1);
         const int stage = (int)(i % kF_Stages);
         const uint32_t phase = (uint32_t)(i / kF_Stages) & 1u;
-        // decoded codes of this step into a_dec[buf] (k-major: [k][row]), scale into a_scl[buf]
-        {
-            const float2 v = FMT == FMT_E4M3 ? decode2_e4m3(raw_c) : decode2_e2m1(raw_c);
-            float* d = a_dec + buf * (kF_KStep * kF_Rows);
-            d[(2 * aj) * kF_Rows + am] = v.x;
-            d[(2 * aj + 1) * kF_Rows + am] = v.y;
-            if (aj == 0) a_scl[buf * kF_Rows + am] = block_scale(raw_s);
-        }
         Unit nx = w;
         nx.next(p);
-        if (u + 1 < u1) load_a_raw<FMT>(p, nx, am, aj, raw_c, raw_s);  // used one step later
-        // a_dec[buf] complete; every thread is also past its reads of a_dec[buf]
-        // from two steps ago (it reached this barrier one step ago)
-        named_bar_sync(1, 32 * kF_Workers);
         if (live) live = mbar_wait(&full[stage], phase, p.wait_limit_ns, p.err);
         if (live) {
             const uint8_t* bs = smem + stage * kF_StageBytes + b_off;
-            const float* as = a_dec + buf * (kF_KStep * kF_Rows) + rg * kF_TM;
-            float blk[kF_TM][4];
+            const float* as = a_dec + stage * (kF_KStep * kF_Rows) + rg * kF_TM;
+            // packed pairs of rows (r, r+1): two f32 lanes per fma.rn.f32x2
+            unsigned long long blk2[kF_TM / 2][4];
+            float4 bn = *reinterpret_cast<const float4*>(bs);
+            float4 an[kF_TM / 4];
+#pragma unroll
+            for (int r = 0; r < kF_TM / 4; ++r) an[r] = *reinterpret_cast<const float4*>(as + 4 * r);
 #pragma unroll
             for (int k = 0; k < kF_KStep; ++k) {
-                const float4 b = *reinterpret_cast<const float4*>(bs + k * (kF_Half * 4));
-                float a[kF_TM];
+                const float4 b = bn;
+                unsigned long long ap[kF_TM / 2], bd[4];
 #pragma unroll
-                for (int r = 0; r < kF_TM; r += 4) {
-                    const float4 q = *reinterpret_cast<const float4*>(as + k * kF_Rows + r);
-                    a[r] = q.x;
-                    a[r + 1] = q.y;
-                    a[r + 2] = q.z;
-                    a[r + 3] = q.w;
+                for (int r = 0; r < kF_TM / 4; ++r) {
+                    ap[2 * r] = pk2(an[r].x, an[r].y);
+                    ap[2 * r + 1] = pk2(an[r].z, an[r].w);
+                }
+                bd[0] = pk2(b.x, b.x);
+                bd[1] = pk2(b.y, b.y);
+                bd[2] = pk2(b.z, b.z);
+                bd[3] = pk2(b.w, b.w);
+                if (k + 1 < kF_KStep) {
+                    bn = *reinterpret_cast<const float4*>(bs + (k + 1) * (kF_Box * 4));
+#pragma unroll
+                    for (int r = 0; r < kF_TM / 4; ++r)
+                        an[r] = *reinterpret_cast<const float4*>(as + (k + 1) * kF_Rows + 4 * r);
                 }
 #pragma unroll
-                for (int r = 0; r < kF_TM; ++r) {
-                    if (k == 0) {
-                        blk[r][0] = a[r] * b.x;
-                        blk[r][1] = a[r] * b.y;
-                        blk[r][2] = a[r] * b.z;
-                        blk[r][3] = a[r] * b.w;
-                    } else {
-                        blk[r][0] = fmaf(a[r], b.x, blk[r][0]);
-                        blk[r][1] = fmaf(a[r], b.y, blk[r][1]);
-                        blk[r][2] = fmaf(a[r], b.z, blk[r][2]);
-                        blk[r][3] = fmaf(a[r], b.w, blk[r][3]);
-                    }
-                }
+                for (int r = 0; r < kF_TM / 2; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) blk2[r][c] = k == 0 ? mul2(ap[r], bd[c]) : fma2(ap[r], bd[c], blk2[r][c]);
             }
+            unsigned long long sc2[kF_TM / 2];
+#pragma unroll
+            for (int r = 0; r < kF_TM / 2; ++r)
+                sc2[r] = pk2(a_scl[stage * kF_Rows + rg * kF_TM + 2 * r], a_scl[stage * kF_Rows + rg * kF_TM + 2 * r + 1]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (lane == 0) mbar_arrive(&empty[stage]);  // B stage and A slot both read
 #pragma unroll
-            for (int r = 0; r < kF_TM; ++r) {
-                const float sc = a_scl[buf * kF_Rows + rg * kF_TM + r];
+            for (int r = 0; r < kF_TM / 2; ++r)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(blk[r][c], sc, acc[r][c]);
-            }
+                for (int c = 0; c < 4; ++c) {
+                    unsigned long long a2 = pk2(acc[2 * r][c], acc[2 * r + 1][c]);
+                    a2 = fma2(blk2[r][c], sc2[r], a2);
+                    unpk2(a2, acc[2 * r][c], acc[2 * r + 1][c]);
+                }
         }
         if (u + 1 == u1 || !nx.same_tile(w)) {
             // end of this CTA's share of the tile: add the partial sums into C
@@ -311,8 +393,8 @@ cudaError_t launch_block_matmul_f32b(const GemmF32bArgs& a, cudaStream_t stream,
     p.a_layout = a.a_layout;
     p.MT = (int)((a.M + kF_Rows - 1) / kF_Rows);
     p.NT = (int)((a.N + kF_Cols - 1) / kF_Cols);
-    p.KB = (int)(a.K / kF_KStep);
-    p.total = (int64_t)p.MT * p.NT * p.KB;
+    p.KS = (int)(a.K / kF_KStep);
+    p.total = (int64_t)p.MT * p.NT * p.KS;
     p.C = a.C;
     p.wait_limit_ns = wait_limit_ns();
     p.err = device_error_word();
@@ -323,13 +405,14 @@ cudaError_t launch_block_matmul_f32b(const GemmF32bArgs& a, cudaStream_t stream,
     CUtensorMap tm;
     const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.K};
     const uint64_t strides[1] = {(uint64_t)a.N * 4};
-    const uint32_t box[2] = {(uint32_t)kF_Half, (uint32_t)kF_KStep};
+    const uint32_t box[2] = {(uint32_t)kF_Box, (uint32_t)kF_KStep};
     if (!encode_tiled_map(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.B, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) {
         *detail = "cuTensorMapEncodeTiled rejected B";
         return cudaErrorInvalidValue;
     }
-    const int grid = (int)(p.total < sm_count() ? p.total : sm_count());
+    const int64_t slots = (int64_t)kF_CtasPerSm * sm_count();
+    const int grid = (int)(p.total < slots ? p.total : slots);
     return a.a_fmt == FMT_E2M1 ? run_f32b<FMT_E2M1>(tm, p, grid, stream) : run_f32b<FMT_E4M3>(tm, p, grid, stream);
 }
 
