@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>:
     using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
     constexpr int ACC = C_::ACC;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by an offset from the array itself: the compiler then keeps the
+    // generic accesses below (epilogue staging, activation tiles) in the shared window
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C_::OFF_BAR);
     uint64_t* empty = full + STAGES;
     uint64_t* tmem_full = empty + STAGES;   // [ACC]
@@ -829,7 +831,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
     using C_ = PairCfg<KIND, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     // the same offsets in both CTAs: the MMAs and barrier addresses rely on it
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by an offset from the array itself: the compiler then keeps the
+    // generic accesses below (epilogue staging, activation tiles) in the shared window
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C_::OFF_BAR);  // used in the even CTA
     uint64_t* empty = full + STAGES;
     uint64_t* tmem_full = empty + STAGES;
