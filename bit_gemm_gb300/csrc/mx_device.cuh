@@ -172,6 +172,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* 
         : "memory");
 }
 
+// 2-D tiled tensor store shared -> global (bulk group completion); elements
+// outside the tensor are not written.  Coordinates must be non-negative.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group"
+        " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(x), "r"(y), "r"(smem_u32(src))
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 template <int N>

@@ -447,12 +447,9 @@ __global__ void __launch_bounds__(kThreads) quantize_axis0_kernel(const InT* __r
                 uint32_t out[kCodeWords];
                 const uint32_t sbyte = quantize_column_block<FMT>(u[c], sizeof(InT) == 2, out);
                 uint8_t* dst = codes + col * code_row + (FMT == FMT_E2M1 ? r0 / 2 : r0);
-                if (FMT == FMT_E2M1) {
-                    __stcs(reinterpret_cast<uint4*>(dst), make_uint4(out[0], out[1], out[2], out[3]));
-                } else {
-                    __stcs(reinterpret_cast<uint4*>(dst), make_uint4(out[0], out[1], out[2], out[3]));
-                    __stcs(reinterpret_cast<uint4*>(dst) + 1, make_uint4(out[4], out[5], out[6], out[7]));
-                }
+                // write-back stores: the rest of each line comes from the next blocks
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                if (FMT == FMT_E4M3) reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
                 const int64_t off = LAYOUT == LAYOUT_MMA ? mma_scale_offset(col, b0 + bi, nb4) : col * nb + b0 + bi;
                 scales[off] = (uint8_t)sbyte;
             }
@@ -633,6 +630,8 @@ cudaError_t axis0_fmt(const InT* x, int64_t rows, int64_t cols, int fmt, uint8_t
 
 cudaError_t launch_quantize_axis0(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, void* codes,
                                   uint8_t* scales, int layout, cudaStream_t st) {
+    if (quantize_axis0_tiled_applies(x, dtype, cols))
+        return launch_quantize_axis0_tiled(x, dtype, rows, cols, fmt, codes, scales, layout, st);
     uint8_t* c = static_cast<uint8_t*>(codes);
     if (dtype == DT_F32) return axis0_fmt<float, 1>(static_cast<const float*>(x), rows, cols, fmt, c, scales, layout, st);
     const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(x);

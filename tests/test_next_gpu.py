@@ -64,6 +64,18 @@ def test_axis0_shapes(fmt, dtype, layout):
 
 
 @pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("layout", [mx.SCALES_ROWMAJOR, mx.SCALES_MMA])
+def test_axis0_tiled_shapes(fmt, dtype, layout):
+    # rows of 16-byte multiples take the shared-memory tile path: ragged last
+    # column tiles (264, 520, 1000 columns), one block row, many units per CTA
+    rng = np.random.default_rng(13)
+    for rows, cols in [(32, 8), (64, 264), (96, 520), (1024, 1000), (2048, 4096)]:
+        x = torch.from_numpy(rand(rng, (rows, cols))).to(dtype)
+        check_axis0(x, fmt, layout)
+
+
+@pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
 def test_axis0_every_bf16_pattern_at_every_scale(fmt):
     # the exhaustive bf16 ladder of the last-axis tests, transposed: each
     # column is one block sequence, so axis-0 blocks are the ladder's blocks
