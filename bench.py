@@ -303,7 +303,13 @@ def bench_e2e(mx, hl, steps, world):
             "h2d_bytes_per_step": rows * cols * 2, "d2h_bytes_per_step": rows * cols * 4, "steps": n}
 
 
-def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0):
+def mma_rates(mx):
+    """Measured block-scaled MMA rate per kind (shared-memory operands, no HBM
+    traffic): reported beside the recipe-derived tensor peaks."""
+    return {"fp8": mx.mx_measure_mma_rate(mx.E4M3FN, 20000), "fp4": mx.mx_measure_mma_rate(mx.E2M1, 20000)}
+
+
+def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma=None):
     """block_matmul workloads.  Weights are quantized before timing; the step
     includes the activation quantize where the workload quantizes on the fly."""
     w = workloads.make(cfg, scale=scale)
@@ -383,6 +389,9 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0):
         "tensor_peak_tflops": peak_tf, "tensor_frac": tf_gemm / peak_tf,
         "gemm_gbs": gbs_gemm, "hbm_frac": gbs_gemm / peaks["hbm_gbs"], "gemm_bytes": gemm_bytes,
         "launches_per_step": 2 if quant_a else 1, "nsets": nsets, "clocks": clk.summary()}
+    if mma is not None:
+        out["mma_measured_tflops"] = mma[kind]
+        out["tensor_frac_of_mma_measured"] = tf_gemm / mma[kind]
     if sec_f is not None:
         # one launch: activations in (f32/bf16), weight codes and scales, C read and written
         fused_bytes = a_bytes_in + mx.mx_codes_bytes(fb, N, K) + mx.mx_scales_bytes(L, N, K) + 8 * M * N
@@ -597,16 +606,18 @@ def main():
             out = bench_next(mx, args.steps, args.warmup, world, peaks, dev_index)
         else:
             cfg = {"decode": 3, "square": 4, "prefill": 5}[args.only]
-            out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale, dev_index)
+            out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale, dev_index, mma_rates(mx))
         if rank == 0:
             print(json.dumps(out, default=str), flush=True)
         return
     hl = bench_headline(mx, args.steps, args.warmup, world, peaks, dev_index)
     e2e = bench_e2e(mx, hl, args.steps, world)
     gemms = []
+    mma = None
     if not args.no_gemm:
+        mma = mma_rates(mx)
         for cfg in (3, 4, 5):
-            gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks, 1.0, dev_index))
+            gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks, 1.0, dev_index, mma))
     nxt = None if args.no_gemm else bench_next(mx, args.gemm_steps, max(3, args.warmup), world, peaks, dev_index)
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -629,6 +640,11 @@ def main():
                      "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"},
         "kernels": {"quantize": hl["quantize"], "dequantize": hl["dequantize"]},
         "block_matmul": gemms,
+        "tensor_peaks_tflops": {
+            "recipe_fp8": peaks["bf16_tflops"] * NOMINAL_RATIO["fp8"],
+            "recipe_fp4": peaks["bf16_tflops"] * NOMINAL_RATIO["fp4"],
+            "mma_measured_fp8": mma["fp8"] if mma else None, "mma_measured_fp4": mma["fp4"] if mma else None,
+            "used": "recipe (measured bf16 x nominal ratio); the measured MMA rates are reported beside it"},
         "next": nxt,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     L.mx_block_matmul_act.restype = i32
     L.mx_block_matmul_f32b.argtypes = [vp, vp, i32, i32, i32, i32, vp, i64, i64, i64, vp, vp]
     L.mx_block_matmul_f32b.restype = i32
+    L.mx_measure_mma_rate.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_double), vp]
+    L.mx_measure_mma_rate.restype = i32
     L.mx_device_status.argtypes = [vp]
     L.mx_device_status.restype = i32
     L.mx_selftest_wait_timeout.argtypes = [u64, vp]
@@ -276,6 +278,13 @@ def mx_block_matmul_f32b(a_codes: torch.Tensor, a_scales: torch.Tensor, a_fmt: i
     _check(lib.mx_block_matmul_f32b(_dev_ptr(a_codes, "a_codes", cb), _dev_ptr(a_scales, "a_scales", sb), a_fmt,
                                     scale_layout, block_size, scale_type, _dev_ptr(B, "B", K * N * 4), M, N, K,
                                     _dev_ptr(C, "C", M * N * 4), _stream(stream)))
+
+
+def mx_measure_mma_rate(fmt: int, iters: int = 20000, stream=None) -> float:
+    """Measured block-scaled MMA rate (TFLOP/s, all SMs) for E4M3FN (kind::mxf8f6f4) or E2M1 (kind::mxf4)."""
+    out = ctypes.c_double(0.0)
+    _check(lib.mx_measure_mma_rate(fmt, iters, ctypes.byref(out), _stream(stream)))
+    return out.value
 
 
 def mx_scales_relayout(src: torch.Tensor, src_layout: int, rows: int, cols: int, dst: torch.Tensor,

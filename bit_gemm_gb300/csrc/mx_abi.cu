@@ -302,6 +302,18 @@ mx_status_t mx_block_matmul_f32b(const void* a_codes, const uint8_t* a_scales, m
     return ok();
 }
 
+mx_status_t mx_measure_mma_rate(mx_format_t fmt, int iters, double* tflops, void* stream) {
+    if (!valid_fmt(fmt)) return fail(MX_ERR_UNSUPPORTED, "element format %d", (int)fmt);
+    if (iters < 1 || iters > 1000000) return fail(MX_ERR_SHAPE, "iters %d outside 1..1000000", iters);
+    if (!tflops) return fail(MX_ERR_NULL, "tflops must be non-NULL");
+    mx_status_t s;
+    if ((s = check_device()) != MX_OK) return s;
+    cudaError_t e = mx::measure_mma_rate(fmt == MX_E2M1 ? 1 : 0, iters, tflops, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorLaunchTimeout) return fail(MX_ERR_TIMEOUT, "an MMA-rate CTA gave up waiting for its commit");
+    if (e != cudaSuccess) return cuda_fail(e, "MMA-rate measurement");
+    return ok();
+}
+
 mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
                             const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
                             int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,

@@ -85,6 +85,10 @@ bool encode_tiled_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, con
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                       CUtensorMapSwizzle swizzle);
 
+// Measured rate (TFLOP/s over all SMs) of the block-scaled MMA, kind 0 =
+// kind::mxf8f6f4 (E4M3), 1 = kind::mxf4 (E2M1); synchronous on `stream`.
+cudaError_t measure_mma_rate(int kind, int iters, double* tflops, cudaStream_t stream);
+
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 // Limit (ns) for every bounded wait inside the library's kernels.

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (mx_\w+)", out))
     for n in names:
@@ -217,3 +217,12 @@ def test_block_matmul_f32b_validation():
     assert gf(M=0) == OK and gf(K=0) == OK
     if not torch.cuda.is_available():
         assert gf() == NODEV
+
+
+def test_measure_mma_rate_validation():
+    out = ctypes.c_double(0.0)
+    assert L.mx_measure_mma_rate(3, 10, ctypes.byref(out), None) == UNSUP
+    assert L.mx_measure_mma_rate(mx.E2M1, 0, ctypes.byref(out), None) == SHAPE
+    assert L.mx_measure_mma_rate(mx.E2M1, 10, None, None) == NULL
+    if not torch.cuda.is_available():
+        assert L.mx_measure_mma_rate(mx.E2M1, 10, ctypes.byref(out), None) == NODEV

@@ -204,3 +204,14 @@ def test_workload4_square_mxfp8_sampled():
 def test_workload5_prefill_mxfp4_sampled():
     w = workloads.make(5)
     sampled_check(w["A"], w["W"], mx.E2M1, mx.E2M1, w["C0"], seed=5)
+
+
+def test_measure_mma_rate():
+    # the tensor pipe on shared-memory operands: somewhere between a quarter of
+    # and twice the nominal dense rates (4.5 PF FP8, 13.5 PF FP4)
+    f8 = mx.mx_measure_mma_rate(mx.E4M3FN, 2000)
+    f4 = mx.mx_measure_mma_rate(mx.E2M1, 2000)
+    mx.mx_device_status()
+    assert 1000 < f8 < 9000, f8
+    assert 2000 < f4 < 27000, f4
+    assert f4 > 1.5 * f8
