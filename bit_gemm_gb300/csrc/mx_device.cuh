@@ -32,6 +32,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31) == 0; }
 
+// ------------------------------------------------ programmatic dependent launch
+//
+// A kernel launched with programmatic stream serialization may start (its
+// CTAs resident, their set-up running) before the previous kernel in the
+// stream has finished, once every CTA of that kernel has called
+// launch_dependents or exited.  Before its first access to global memory it
+// waits for the previous kernel to complete and its writes to become visible;
+// without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>:
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned* err = &g_mx_device_error;
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -298,6 +299,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>:
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // set-up above overlaps the previous kernel's tail; global memory from here on
+    pdl_wait();
 
     // K stages this CTA touches (the hull of its work units), for the
     // resident activations
@@ -848,6 +851,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
     const uint32_t pair = cluster_id_x();
     const uint32_t npairs = cluster_count_x();
     unsigned* err = &g_mx_device_error;
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -874,6 +878,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
     cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA use
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // set-up above overlaps the previous kernel's tail; global memory from here on
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -1280,8 +1286,7 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
         if (e != cudaSuccess) return e;
         configured_for = C_::SMEM;
     }
-    kern<<<grid, C_::THREADS, C_::SMEM, st>>>(ta, tb, tsa, tsb, tc, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
 // CTA pairs that can be resident at once for a pair-kernel instantiation
@@ -1291,8 +1296,7 @@ cudaError_t run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
                      const CUtensorMap& tc, const GemmParams& p, int pairs, cudaStream_t st) {
     using C_ = PairCfg<KIND, STAGES>;
     auto kern = gemm_pair_kernel<KIND, STAGES>;
-    kern<<<2 * pairs, C_::THREADS, C_::SMEM, st>>>(ta, tb, tsa, tsb, tc, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(2 * pairs), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
 template <int KIND, int STAGES>

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kF_Threads, kF_CtasPerSm) gemm_f32b_kernel(con
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kF_OffBar);
     uint64_t* empty = full + kF_Stages;
 
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t u0 = p.total * blockIdx.x / gridDim.x, u1 = p.total * (blockIdx.x + 1) / gridDim.x;
 
@@ -227,6 +228,7 @@ __global__ void __launch_bounds__(kF_Threads, kF_CtasPerSm) gemm_f32b_kernel(con
         fence_mbarrier_init();
     }
     __syncthreads();
+    pdl_wait();  // set-up above overlaps the previous kernel's tail
     if (u0 >= u1) return;
 
     if (warp == 0) {
@@ -374,8 +376,7 @@ cudaError_t run_f32b(const CUtensorMap& tm, const F32bParams& p, int grid, cudaS
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid, kF_Threads, kF_Smem, st>>>(tm, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kF_Threads), kF_Smem, st, tm, p);
 }
 
 }  // namespace

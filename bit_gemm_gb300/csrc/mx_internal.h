@@ -6,7 +6,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace mx {
+
+// Launch with programmatic stream serialization (see pdl_wait in
+// mx_device.cuh): the kernel may be scheduled while its predecessor in the
+// stream drains, and must call pdl_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 enum Fmt : int { FMT_E2M1 = 1, FMT_E4M3 = 2 };
 enum Layout : int { LAYOUT_ROWMAJOR = 0, LAYOUT_MMA = 1 };

@@ -97,6 +97,8 @@ template <int FMT, int LAYOUT, int kU>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     quantize_bf16_block_kernel(const __nv_bfloat16* __restrict__ x, int64_t nblocks, int64_t nb, int64_t rows,
                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    pdl_launch_dependents();  // the next kernel may set up while this one runs
+    pdl_wait();               // the previous kernel's writes are visible
     constexpr int kCodeWords = FMT == FMT_E2M1 ? 4 : 8;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const int64_t nb4 = round_up(nb, 4);
@@ -150,6 +152,8 @@ template <typename InT, int FMT, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) quantize_kernel(const InT* __restrict__ x, int64_t nblocks, int64_t nb,
                                                             int64_t rows, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ scales) {
+    pdl_launch_dependents();  // the next kernel may set up while this one runs
+    pdl_wait();               // the previous kernel's writes are visible
     // 64 bytes of input in flight per thread: 4 items of bf16, 2 of f32 (2 when
     // the tensor-core scale layout's index arithmetic needs the registers)
     constexpr int kU = (sizeof(InT) == 2 && LAYOUT == LAYOUT_ROWMAJOR) ? kUnroll : kUnroll / 2;
@@ -286,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) dequantize_kernel(const 
                                                                           const uint8_t* __restrict__ scales,
                                                                           int64_t nblocks, int64_t nb,
                                                                           void* __restrict__ yv) {
+    pdl_launch_dependents();  // the next kernel may set up while this one runs
+    pdl_wait();               // the previous kernel's writes are visible
     float* __restrict__ y = static_cast<float*>(yv);
     const int lane = threadIdx.x & 31;
     const int64_t nwin = (nblocks + 7) / 8;
@@ -504,11 +510,9 @@ cudaError_t quant_dispatch_layout(const InT* x, int64_t nblocks, int64_t nb, int
                 const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
                 const int64_t g2 = grid_for(pad, kMinBlocks);
                 g = g > g2 ? g : g2;
-                quantize_bf16_block_kernel<FMT, LAYOUT_MMA, kU><<<(unsigned)g, kThreads, 0, st>>>(x, nblocks, nb, rows,
-                                                                                                codes, scales);
+                (void)launch_pdl(quantize_bf16_block_kernel<FMT, LAYOUT_MMA, kU>, dim3((unsigned)g), dim3(kThreads), 0, st, x, nblocks, nb, rows, codes, scales);
             } else {
-                quantize_bf16_block_kernel<FMT, LAYOUT_ROWMAJOR, kU><<<(unsigned)g, kThreads, 0, st>>>(
-                    x, nblocks, nb, rows, codes, scales);
+                (void)launch_pdl(quantize_bf16_block_kernel<FMT, LAYOUT_ROWMAJOR, kU>, dim3((unsigned)g), dim3(kThreads), 0, st, x, nblocks, nb, rows, codes, scales);
             }
             return cudaGetLastError();
         }
@@ -517,10 +521,9 @@ cudaError_t quant_dispatch_layout(const InT* x, int64_t nblocks, int64_t nb, int
         const int64_t pad = (round_up(rows, 128) - rows) * round_up(nb, 4) + rows * (round_up(nb, 4) - nb);
         const int64_t g2 = grid_for(pad, 8);
         grid = grid > g2 ? grid : g2;
-        quantize_kernel<InT, FMT, LAYOUT_MMA><<<(unsigned)grid, kThreads, 0, st>>>(x, nblocks, nb, rows, codes, scales);
+        (void)launch_pdl(quantize_kernel<InT, FMT, LAYOUT_MMA>, dim3((unsigned)grid), dim3(kThreads), 0, st, x, nblocks, nb, rows, codes, scales);
     } else {
-        quantize_kernel<InT, FMT, LAYOUT_ROWMAJOR><<<(unsigned)grid, kThreads, 0, st>>>(x, nblocks, nb, rows, codes,
-                                                                                      scales);
+        (void)launch_pdl(quantize_kernel<InT, FMT, LAYOUT_ROWMAJOR>, dim3((unsigned)grid), dim3(kThreads), 0, st, x, nblocks, nb, rows, codes, scales);
     }
     return cudaGetLastError();
 }
@@ -530,14 +533,14 @@ cudaError_t deq_dispatch(const uint8_t* c, const uint8_t* scales, int64_t nblock
                          float* y, unsigned grid, cudaStream_t st) {
     if (fmt == FMT_E2M1) {
         if (layout == LAYOUT_MMA)
-            dequantize_kernel<FMT_E2M1, LAYOUT_MMA, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E2M1, LAYOUT_MMA, kV8>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
         else
-            dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR, kV8>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
     } else {
         if (layout == LAYOUT_MMA)
-            dequantize_kernel<FMT_E4M3, LAYOUT_MMA, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E4M3, LAYOUT_MMA, kV8>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
         else
-            dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR, kV8><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR, kV8>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
     }
     return cudaGetLastError();
 }
@@ -583,14 +586,14 @@ cudaError_t launch_dequantize_bf16(const void* codes, const uint8_t* scales, int
     const uint8_t* c = static_cast<const uint8_t*>(codes);
     if (fmt == FMT_E2M1) {
         if (layout == LAYOUT_MMA)
-            dequantize_kernel<FMT_E2M1, LAYOUT_MMA, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E2M1, LAYOUT_MMA, false, true>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
         else
-            dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E2M1, LAYOUT_ROWMAJOR, false, true>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
     } else {
         if (layout == LAYOUT_MMA)
-            dequantize_kernel<FMT_E4M3, LAYOUT_MMA, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E4M3, LAYOUT_MMA, false, true>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
         else
-            dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR, false, true><<<grid, kThreads, 0, st>>>(c, scales, nblocks, nb, y);
+            (void)launch_pdl(dequantize_kernel<FMT_E4M3, LAYOUT_ROWMAJOR, false, true>, dim3(grid), dim3(kThreads), 0, st, c, scales, nblocks, nb, y);
     }
     return cudaGetLastError();
 }

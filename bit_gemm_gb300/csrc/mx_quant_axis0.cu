@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kX_Threads, (AxisCfg<InT, FMT>::kCtas))
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cf::kOffBar);
     uint64_t* empty = full + Cf::kStages;
 
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t u0 = p.total * blockIdx.x / gridDim.x, u1 = p.total * (blockIdx.x + 1) / gridDim.x;
     if (threadIdx.x == 0) {
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kX_Threads, (AxisCfg<InT, FMT>::kCtas))
         fence_mbarrier_init();
     }
     __syncthreads();
+    pdl_wait();  // set-up above overlaps the previous kernel's tail
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA
@@ -199,8 +201,7 @@ cudaError_t run_axis0(const CUtensorMap& tx, const CUtensorMap& tc, const Axis0P
     }
     const int64_t slots = (int64_t)Cf::kCtas * sm_count();
     const int grid = (int)(p.total < slots ? p.total : slots);
-    kern<<<grid, kX_Threads, Cf::kSmem, st>>>(tx, tc, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kX_Threads), Cf::kSmem, st, tx, tc, p);
 }
 
 template <typename InT>
