@@ -131,12 +131,17 @@ __device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint3
     return true;
 }
 
-template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0>
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0, int SA = 1>
 struct Cfg {
+    // SA: K atoms (128 bytes of K per operand row) per pipeline stage; a stage
+    // of SA atoms is loaded with one 3-D box per operand and scale tensor, so
+    // per-stage costs (barrier round trips, load issue) are paid once per SA
+    // atoms.  SA > 1 needs K a whole number of stages and tensor-core scales.
     // ACT_ATOMS > 0: the activations (the MMA B operand of a swapped shape) are
     // quantized by the kernel into a resident region of that many K stages
     static constexpr bool ACT = ACT_ATOMS > 0;
-    static constexpr int G = KIND == KIND_F4 ? 2 : 1;                 // scale groups per stage
+    static constexpr int G = KIND == KIND_F4 ? 2 : 1;                 // scale groups per atom
+    static constexpr int GS = SA * G;                                  // scale groups per stage
     // 128-row scale tiles covering the BN rows of a B tile (tiles start on
     // 128-row boundaries: scale-factor TMEM addresses must stay aligned)
     static constexpr int SFB_TILES = (BN + 127) / 128;
@@ -148,15 +153,17 @@ struct Cfg {
     static constexpr int EPI_WARPS = (!SWAP && BN == 256) ? 8 : 4;
     static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
     static constexpr int THREADS = 32 * (GATE_WARP + 1);
-    static constexpr int A_BYTES = kBlockM * kRowBytes;               // 16 KB
-    static constexpr int B_BYTES = ACT ? 0 : BN * kRowBytes;
-    static constexpr int SFA_BYTES = G * 512;
-    static constexpr int SFB_BYTES = ACT ? 0 : G * SFB_TILES * 512;
+    static constexpr int A_ATOM = kBlockM * kRowBytes;                // 16 KB
+    static constexpr int B_ATOM = BN * kRowBytes;
+    static constexpr int A_BYTES = SA * A_ATOM;
+    static constexpr int B_BYTES = ACT ? 0 : SA * B_ATOM;
+    static constexpr int SFA_BYTES = GS * 512;
+    static constexpr int SFB_BYTES = ACT ? 0 : GS * SFB_TILES * 512;
     static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);  // full scale boxes of a stage
     static constexpr int ACT_BYTES = BN * kRowBytes;  // one resident K stage of the activations
     static constexpr int ACT_SF_BYTES = G * 512;
-    static constexpr int SF_COLS_A = 4 * G;
-    static constexpr int SF_COLS_B = 4 * G * SFB_TILES;
+    static constexpr int SF_COLS_A = 4 * GS;
+    static constexpr int SF_COLS_B = 4 * GS * SFB_TILES;
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
     static constexpr int SF_COL0 = ACC * BN > 256 ? ACC * BN : 256;   // first scale column
     // scale slots in TMEM; a slot is rewritten by tcgen05.cp only after the
@@ -188,6 +195,7 @@ struct Cfg {
     static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
     static_assert(STAGES <= 15, "one named barrier per stage");
+    static_assert(SA == 1 || (!ACT && SWAP), "several atoms per stage: swapped shapes with streamed B");
 };
 
 // Write 32 rows x 128 columns of accumulator (this warp's lane quarter, in
@@ -246,12 +254,12 @@ __device__ __forceinline__ void epilogue_write_128(const GemmParams& p, const CU
     }
 }
 
-template <int KIND, int BN, int STAGES, int SWAP, int NBUF_, int ACT_ATOMS = 0>
-__global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>::THREADS, 1)
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_, int ACT_ATOMS = 0, int SA = 1>
+__global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, SA>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                 const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
+    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, SA>;
     constexpr int ACC = C_::ACC;
     extern __shared__ uint8_t smem_raw[];
     // aligned by an offset from the array itself: the compiler then keeps the
@@ -471,8 +479,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>:
                     const int kbg = kb + p.k_atom0;  // stage of K in the whole tensor
                     const int nl = (C_::ACT || p.sf_rowmajor) ? 2 : 4;
                     const uint32_t dst = lbase + (uint32_t)stage * lstep;
-                    const int32_t y = li == 0 ? p0 : li == 1 ? q0 : 4 * C_::G * kbg;
-                    const int32_t z = li < 2 ? kbg : (li == 2 ? w.tp : q0 >> 7);
+                    const int32_t y = li == 0 ? p0 : li == 1 ? q0 : 4 * C_::GS * kbg;
+                    const int32_t z = li < 2 ? SA * kbg : (li == 2 ? w.tp : q0 >> 7);
                     if (lane < nl) {
                         if (p.op3d || li >= 2) tma_load_3d_at(dst, lmap, 0, y, z, &full[stage]);
                         else tma_load_2d_at(dst, lmap, kbg * kRowBytes, y, &full[stage]);
@@ -538,7 +546,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>:
             const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
             idesc[i] = p.idesc | (sf_id << 4) | (sf_id << 29);
         }
-        constexpr int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
+        constexpr int k_elem_per_stage = SA * (KIND == KIND_F4 ? 256 : 128);
         constexpr int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
         int stage = 0;
         int sf_slot = 0;
@@ -574,28 +582,35 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>:
                     const int g_first = (kb + p.k_atom0) * C_::G;
                     // valid MMAs in this stage (ragged K): each consumes 32 bytes of K
                     const int rem = p.K - (kb + p.k_atom0) * k_elem_per_stage;
-                    if (rem >= k_elem_per_stage) {
+                    if (SA > 1 || rem >= k_elem_per_stage) {
                         // full stage: everything unrolled.
                         // scale tiles -> TMEM: SFA group g at sf_col + 4g;
                         // SFB group g, row-tile t at sf_col + SF_COLS_A + 4(g*SFB_TILES + t)
+                        // (g counts the stage's groups: atom a holds groups a*G ..)
 #pragma unroll
-                        for (int g = 0; g < C_::G; ++g) {
+                        for (int g = 0; g < C_::GS; ++g) {
                             tc_cp_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
 #pragma unroll
                             for (int t = 0; t < C_::SFB_TILES; ++t)
                                 tc_cp_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (g * C_::SFB_TILES + t),
-                                                     sfb_desc + (t * C_::G + g) * 32);
+                                                     sfb_desc + (t * C_::GS + g) * 32);
                         }
 #pragma unroll
-                        for (int i = 0; i < kMmaPerStage; ++i) {
-                            const int g = KIND == KIND_F4 ? (i >> 1) : 0;
-                            const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
-                            if (KIND == KIND_F4)
-                                mma_mxf4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
-                                         sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
-                            else
-                                mma_mxf8f6f4(d_tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                        for (int a = 0; a < SA; ++a) {
+                            // atom a of the stage: its A and B rows follow the previous atom's
+                            const uint64_t ad = a_desc + a * (C_::A_ATOM >> 4);
+                            const uint64_t bd = b_desc + a * (C_::B_ATOM >> 4);
+#pragma unroll
+                            for (int i = 0; i < kMmaPerStage; ++i) {
+                                const int g = a * C_::G + (KIND == KIND_F4 ? (i >> 1) : 0);
+                                const uint32_t accum = (kb > w.kb0 || a > 0 || i > 0) ? 1u : 0u;
+                                if (KIND == KIND_F4)
+                                    mma_mxf4(d_tmem, ad + 2 * i, bd + 2 * i, idesc[i], sf_col + 4 * g,
                                              sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
+                                else
+                                    mma_mxf8f6f4(d_tmem, ad + 2 * i, bd + 2 * i, idesc[i], sf_col + 4 * g,
+                                                 sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
+                            }
                         }
                     } else {
                         // the ragged last stage of K
@@ -1195,7 +1210,8 @@ bool make_operand_map(CUtensorMap* m, const void* codes, int64_t rows, int64_t K
 // and the row stride a row's bytes, so the box {atom, box_rows, 1} at
 // (0, row, stage) is the 2-D box at (128 B * stage, row).  Only for K a whole
 // number of stages: a partial last atom would read into the next row.
-bool make_operand_map3(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int fmt_kind, int box_rows) {
+bool make_operand_map3n(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int fmt_kind, int box_rows,
+                        int box_atoms) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -1218,12 +1234,16 @@ bool make_operand_map3(CUtensorMap* m, const void* codes, int64_t rows, int64_t 
         strides[1] = kRowBytes / 2;
     }
     dims[1] = (cuuint64_t)rows;
-    cuuint32_t box[3] = {(cuuint32_t)kRowBytes, (cuuint32_t)box_rows, 1};
+    cuuint32_t box[3] = {(cuuint32_t)kRowBytes, (cuuint32_t)box_rows, (cuuint32_t)box_atoms};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, dt, 3, const_cast<void*>(codes), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_operand_map3(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int fmt_kind, int box_rows) {
+    return make_operand_map3n(m, codes, rows, K, fmt_kind, box_rows, 1);
 }
 
 // Tensor map over C (rows x cols f32, row-major) for the reduce-add epilogue.
@@ -1275,11 +1295,11 @@ bool make_sf_map(CUtensorMap* m, const uint8_t* sf, int64_t rows, int32_t sf_gro
     return r == CUDA_SUCCESS;
 }
 
-template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0>
+template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0, int SA = 1>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                 const CUtensorMap& tc, const GemmParams& p, int grid, cudaStream_t st) {
-    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
-    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS>;
+    using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, SA>;
+    auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, SA>;
     static int configured_for = -1;  // per-instantiation attribute (process-wide; one value for all devices)
     if (configured_for != C_::SMEM) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM);
@@ -1443,12 +1463,18 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
     CUtensorMap ta, tb, tsa, tsb, tc;
     const int op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
-    auto opmap = op3d ? make_operand_map3 : make_operand_map;
+    // decode shapes stream two K atoms per stage when K allows (the stage
+    // count, not the bytes, bounds them)
+    const int sa = (swap && bn <= 32 && a.scale_layout == LAYOUT_MMA && a.K % (2 * k_per_stage) == 0) ? 2 : 1;
+    auto opmap = [&](CUtensorMap* m, const void* codes, int64_t rows, int f, int box_rows) {
+        return op3d ? make_operand_map3n(m, codes, rows, a.K, fk(f), box_rows, sa)
+                    : make_operand_map(m, codes, rows, a.K, fk(f), box_rows);
+    };
     const int32_t sf_groups = (int32_t)(round_up(a.K / 32, 4) / 4);
-    const int gsz = kind == KIND_F4 ? 2 : 1;
+    const int gsz = (kind == KIND_F4 ? 2 : 1) * sa;
     std::memset(&tsa, 0, sizeof(tsa));
     std::memset(&tsb, 0, sizeof(tsb));
-    if (!opmap(&ta, x_codes, P, a.K, fk(x_fmt), kBlockM) || !opmap(&tb, y_codes, Q, a.K, fk(y_fmt), bn) ||
+    if (!opmap(&ta, x_codes, P, x_fmt, kBlockM) || !opmap(&tb, y_codes, Q, y_fmt, bn) ||
         (a.scale_layout == LAYOUT_MMA &&
          (!make_sf_map(&tsa, x_sf, P, sf_groups, gsz, 1) || !make_sf_map(&tsb, y_sf, Q, sf_groups, gsz, (bn + 127) / 128)))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
@@ -1473,7 +1499,7 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     p.K = (int32_t)a.K;
     p.tiles_p = (int32_t)((P + kBlockM - 1) / kBlockM);
     p.tiles_q = (int32_t)((Q + bn - 1) / bn);
-    p.k_stages = (int32_t)((a.K + k_per_stage - 1) / k_per_stage);
+    p.k_stages = (int32_t)((a.K + sa * k_per_stage - 1) / (sa * k_per_stage));
     p.sf_groups = (int32_t)(round_up(a.K / 32, 4) / 4);
     p.wait_limit_ns = wait_limit_ns();
     p.idesc = make_idesc(kind, x_fmt, y_fmt, bn);
@@ -1486,8 +1512,8 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     p.sfb = y_sf;
     // A load of 4-bit codes expanded to one byte each in shared memory
     // (16U4_ALIGN16B) completes with the packed byte count: 64 B per row.
-    p.tx_a = (uint32_t)kBlockM * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
-    p.tx_b = (uint32_t)bn * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.tx_a = (uint32_t)(sa * kBlockM) * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.tx_b = (uint32_t)(sa * bn) * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
     p.sf_rowmajor = a.scale_layout == LAYOUT_ROWMAJOR ? 1 : 0;
     p.nb = (int32_t)(a.K / 32);
     p.op3d = op3d;
@@ -1505,6 +1531,16 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     }
 
 #define MX_RUN(KIND_, BN_, ST_, SW_) return run<KIND_, BN_, ST_, SW_>(ta, tb, tsa, tsb, tc, p, grid, st)
+#define MX_RUN2(KIND_, BN_, ST_) return run<KIND_, BN_, ST_, 1, 0, 0, 2>(ta, tb, tsa, tsb, tc, p, grid, st)
+    if (sa == 2) {
+        if (kind == KIND_F4) {
+            if (bn == 16) MX_RUN2(KIND_F4, 16, 5);
+            MX_RUN2(KIND_F4, 32, 4);
+        }
+        if (bn == 16) MX_RUN2(KIND_F8F6F4, 16, 5);
+        MX_RUN2(KIND_F8F6F4, 32, 4);
+    }
+#undef MX_RUN2
     if (swap) {
         if (kind == KIND_F4) {
             if (bn == 16) MX_RUN(KIND_F4, 16, 10, 1);
