@@ -195,7 +195,7 @@ struct Cfg {
     static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
     static_assert(STAGES <= 15, "one named barrier per stage");
-    static_assert(SA == 1 || (!ACT && SWAP), "several atoms per stage: swapped shapes with streamed B");
+    static_assert(SA == 1 || SWAP, "several atoms per stage: swapped (decode) shapes");
 };
 
 // Write 32 rows x 128 columns of accumulator (this warp's lane quarter, in
@@ -327,16 +327,16 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             // mx_quantize's rounding, into the MMA operand layout: per stage, BN
             // rows of 128 bytes with the 128-byte swizzle, and the scale tile(s).
             // Rows past M and elements past K become zero codes.
-            constexpr int BPA = KIND == KIND_F4 ? 8 : 4;  // 32-element blocks per stage
+            constexpr int BPA = KIND == KIND_F4 ? 8 : 4;  // 32-element blocks per atom
             constexpr int AFMT = KIND == KIND_F4 ? FMT_E2M1 : FMT_E4M3;
             const int nthr = 32 * C_::GATE_WARP;
-            const int64_t items = (int64_t)(kb_hi - kb_lo) * BN * BPA;
-            // block i: stage a, row r, block j of the stage; its first element k
+            const int64_t items = (int64_t)SA * (kb_hi - kb_lo) * BN * BPA;
+            // block i: atom a (of the CTA's range), row r, block j of the atom; its first element k
             auto item = [&](int64_t i, int& a, int& r, int& j, int64_t& k) {
                 j = (int)(i % BPA);
                 r = (int)((i / BPA) % BN);
                 a = (int)(i / (BPA * BN));
-                k = ((int64_t)(p.k_atom0 + kb_lo + a) * BPA + j) * 32;
+                k = (((int64_t)SA * (p.k_atom0 + kb_lo) + a) * BPA + j) * 32;
             };
             auto emit = [&](const uint32_t (&u)[32], bool bf16, int a, int r, int j) {
                 uint32_t out[AFMT == FMT_E2M1 ? 4 : 8];
@@ -574,10 +574,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
                     const uint64_t a_desc = a_desc0 + stage * (C_::A_BYTES >> 4);
                     // B and its scales: the stage's ring slot, or the resident stage kb
-                    const uint64_t b_desc = C_::ACT ? b_desc0 + (kb - kb_lo) * (C_::ACT_BYTES >> 4)
+                    const uint64_t b_desc = C_::ACT ? b_desc0 + (kb - kb_lo) * SA * (C_::ACT_BYTES >> 4)
                                                     : b_desc0 + stage * (C_::B_BYTES >> 4);
                     const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
-                    const uint64_t sfb_desc = C_::ACT ? sfb_desc0 + (kb - kb_lo) * (C_::ACT_SF_BYTES >> 4)
+                    const uint64_t sfb_desc = C_::ACT ? sfb_desc0 + (kb - kb_lo) * SA * (C_::ACT_SF_BYTES >> 4)
                                                       : sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
                     const int g_first = (kb + p.k_atom0) * C_::G;
                     // valid MMAs in this stage (ragged K): each consumes 32 bytes of K
@@ -1568,15 +1568,17 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
 // each CTA quantizes once for the K stages it touches.  K is covered by as
 // many launches as the resident region needs (each adds its part into C).
 namespace {
-template <int KIND, int BN, int STAGES, int ATOMS>
+template <int KIND, int BN, int STAGES, int ATOMS, int SA = 1>
 cudaError_t run_act_chunks(const GemmActArgs& a, const CUtensorMap& ta, const CUtensorMap& tsa, const CUtensorMap& tc,
                            GemmParams p, int64_t total_stages, cudaStream_t st) {
     CUtensorMap none;
     std::memset(&none, 0, sizeof(none));
     const int sms = sm_count();
-    for (int64_t c0 = 0; c0 < total_stages; c0 += ATOMS) {
+    constexpr int kChunk = ATOMS / SA;  // stages of SA atoms that fit the resident region
+    static_assert(ATOMS % SA == 0, "whole stages in the resident region");
+    for (int64_t c0 = 0; c0 < total_stages; c0 += kChunk) {
         p.k_atom0 = (int32_t)c0;
-        p.k_stages = (int32_t)(total_stages - c0 < ATOMS ? total_stages - c0 : ATOMS);
+        p.k_stages = (int32_t)(total_stages - c0 < kChunk ? total_stages - c0 : kChunk);
         const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
         p.total_units = tiles * p.k_stages;
         int grid;
@@ -1587,7 +1589,7 @@ cudaError_t run_act_chunks(const GemmActArgs& a, const CUtensorMap& ta, const CU
             p.mode = 1;
             grid = (int)(p.total_units < sms ? p.total_units : sms);
         }
-        cudaError_t e = run<KIND, BN, STAGES, 1, 0, ATOMS>(ta, none, tsa, none, tc, p, grid, st);
+        cudaError_t e = run<KIND, BN, STAGES, 1, 0, ATOMS, SA>(ta, none, tsa, none, tc, p, grid, st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1615,7 +1617,10 @@ cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t st, const
     p.C = a.C;
     p.ldc = a.N;
     p.sfa = a.w_scales;
-    p.tx_a = (uint32_t)kBlockM * (fk(a.w_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    // two K atoms per stage where K allows (decode shapes: the stage count
+    // bounds them)
+    const int sa = (bn <= 32 && a.K % (2 * k_per_stage) == 0) ? 2 : 1;
+    p.tx_a = (uint32_t)(sa * kBlockM) * (fk(a.w_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
     p.nb = (int32_t)(a.K / 32);
     p.group_p = p.tiles_p;
     p.op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
@@ -1624,14 +1629,24 @@ cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t st, const
     p.act_bf16 = a.act_dtype == DT_BF16 ? 1 : 0;
     CUtensorMap ta, tsa, tc;
     std::memset(&tc, 0, sizeof(tc));
-    auto opmap = p.op3d ? make_operand_map3 : make_operand_map;
-    if (!opmap(&ta, a.w_codes, a.N, a.K, fk(a.w_fmt), kBlockM) ||
-        !make_sf_map(&tsa, a.w_scales, a.N, p.sf_groups, kind == KIND_F4 ? 2 : 1, 1) ||
+    const bool okm = p.op3d ? make_operand_map3n(&ta, a.w_codes, a.N, a.K, fk(a.w_fmt), kBlockM, sa)
+                            : make_operand_map(&ta, a.w_codes, a.N, a.K, fk(a.w_fmt), kBlockM);
+    if (!okm || !make_sf_map(&tsa, a.w_scales, a.N, p.sf_groups, (kind == KIND_F4 ? 2 : 1) * sa, 1) ||
         (p.use_tma_epi && !make_c_map(&tc, a.C, a.M, a.N, 32, bn, 0))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
         return cudaErrorInvalidValue;
     }
-    const int64_t total = (a.K + k_per_stage - 1) / k_per_stage;
+    const int64_t total = (a.K + sa * k_per_stage - 1) / (sa * k_per_stage);
+#define MX_ACT2(KIND_, BN_, ST_, AT_) return run_act_chunks<KIND_, BN_, ST_, AT_, 2>(a, ta, tsa, tc, p, total, st)
+    if (sa == 2) {
+        if (kind == KIND_F4) {
+            if (bn == 16) MX_ACT2(KIND_F4, 16, 3, 32);
+            MX_ACT2(KIND_F4, 32, 3, 16);
+        }
+        if (bn == 16) MX_ACT2(KIND_F8F6F4, 16, 3, 32);
+        MX_ACT2(KIND_F8F6F4, 32, 3, 16);
+    }
+#undef MX_ACT2
 #define MX_ACT(KIND_, BN_, ST_, AT_) return run_act_chunks<KIND_, BN_, ST_, AT_>(a, ta, tsa, tc, p, total, st)
     if (kind == KIND_F4) {
         if (bn == 16) MX_ACT(KIND_F4, 16, 6, 32);
