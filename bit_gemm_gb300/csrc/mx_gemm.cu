@@ -1163,14 +1163,21 @@ bool encode_tiled_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, con
 }
 
 unsigned* device_error_word() {
-    static unsigned* word = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
+    // the symbol's address in the current device's context, looked up once per device
+    static std::mutex mu;
+    static unsigned* word[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!word[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_mx_device_error) == cudaSuccess) word = static_cast<unsigned*>(p);
+        if (cudaGetSymbolAddress(&p, g_mx_device_error) == cudaSuccess) word[dev] = static_cast<unsigned*>(p);
         else cudaGetLastError();
-    });
-    return word;
+    }
+    return word[dev];
 }
 
 namespace {
@@ -1300,12 +1307,8 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
                 const CUtensorMap& tc, const GemmParams& p, int grid, cudaStream_t st) {
     using C_ = Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, SA>;
     auto kern = gemm_kernel<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, SA>;
-    static int configured_for = -1;  // per-instantiation attribute (process-wide; one value for all devices)
-    if (configured_for != C_::SMEM) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM);
-        if (e != cudaSuccess) return e;
-        configured_for = C_::SMEM;
-    }
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
@@ -1316,34 +1319,42 @@ cudaError_t run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
                      const CUtensorMap& tc, const GemmParams& p, int pairs, cudaStream_t st) {
     using C_ = PairCfg<KIND, STAGES>;
     auto kern = gemm_pair_kernel<KIND, STAGES>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(2 * pairs), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
 template <int KIND, int STAGES>
 int pair_capacity() {
     using C_ = PairCfg<KIND, STAGES>;
-    static int cap = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        auto kern = gemm_pair_kernel<KIND, STAGES>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM) != cudaSuccess) {
-            cudaGetLastError();
-            cap = 0;
-            return;
-        }
+    static std::mutex mu;
+    static int cap[64];
+    static bool known[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (known[dev]) return cap[dev];
+    auto kern = gemm_pair_kernel<KIND, STAGES>;
+    int n = 0;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM) == cudaSuccess) {
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2), 1, 1);
         cfg.blockDim = dim3(C_::THREADS, 1, 1);
         cfg.dynamicSmemBytes = C_::SMEM;
-        int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
-        cap = n;
-    });
-    return cap;
+    } else {
+        cudaGetLastError();
+    }
+    cap[dev] = n;
+    known[dev] = true;
+    return n;
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns) {

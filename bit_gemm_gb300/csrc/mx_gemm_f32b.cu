@@ -370,12 +370,8 @@ __global__ void __launch_bounds__(kF_Threads, kF_CtasPerSm) gemm_f32b_kernel(con
 template <int FMT>
 cudaError_t run_f32b(const CUtensorMap& tm, const F32bParams& p, int grid, cudaStream_t st) {
     auto kern = gemm_f32b_kernel<FMT>;
-    static bool configured = false;  // per instantiation
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kF_Smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), kF_Smem);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kF_Threads), kF_Smem, st, tm, p);
 }
 

@@ -6,9 +6,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <set>
 #include <utility>
 
 namespace mx {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device, size).
+inline cudaError_t ensure_smem_limit(const void* kern, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<std::pair<const void*, int>, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(std::make_pair(kern, dev), bytes);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
 
 // Launch with programmatic stream serialization (see pdl_wait in
 // mx_device.cuh): the kernel may be scheduled while its predecessor in the

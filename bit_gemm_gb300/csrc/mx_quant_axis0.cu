@@ -193,12 +193,8 @@ template <typename InT, int FMT, int LAYOUT>
 cudaError_t run_axis0(const CUtensorMap& tx, const CUtensorMap& tc, const Axis0Params& p, cudaStream_t st) {
     using Cf = AxisCfg<InT, FMT>;
     auto kern = quantize_axis0_tiled_kernel<InT, FMT, LAYOUT>;
-    static bool configured = false;  // per instantiation
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), Cf::kSmem);
+    if (e != cudaSuccess) return e;
     const int64_t slots = (int64_t)Cf::kCtas * sm_count();
     const int grid = (int)(p.total < slots ? p.total : slots);
     return launch_pdl(kern, dim3(grid), dim3(kX_Threads), Cf::kSmem, st, tx, tc, p);
