@@ -203,8 +203,12 @@ struct Cfg {
 // TMA reduce-add of 32 x 16 boxes through one 2 KB 64-byte-swizzled staging
 // buffer per warp, or vector / scalar reductions.  Columns past N and rows past
 // M are clipped.
+// EC: columns per TMA box, 16 (64-byte swizzled rows, 2 KB per warp) or 8
+// (unswizzled 32-byte rows, 1 KB per warp, for kernels short of shared memory).
+template <int EC = 16>
 __device__ __forceinline__ void epilogue_write_128(const GemmParams& p, const CUtensorMap& tm_c, const uint32_t (&r)[4][32],
                                                    int32_t p0, int32_t qc, uint8_t* stage_buf, int& nbuf, int lane) {
+    static_assert(EC == 16 || EC == 8, "epilogue box columns");
     const int32_t pr = p0 + lane;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -226,22 +230,31 @@ __device__ __forceinline__ void epilogue_write_128(const GemmParams& p, const CU
             }
         } else if (p.use_tma_epi) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                if (qc + 32 * c + 16 * hh >= p.Q) break;
-                uint8_t* buf = stage_buf;  // one 32 x 16 buffer per warp
+            for (int hh = 0; hh < 32 / EC; ++hh) {
+                if (qc + 32 * c + EC * hh >= p.Q) break;
+                uint8_t* buf = stage_buf;  // one 32 x EC buffer per warp
                 if (nbuf >= 1 && lane == 0) bulk_wait_group_read<0>();
                 __syncwarp();
-                // [32 rows][16 f32], 64-byte swizzle: 16-B chunk j of row i at j ^ ((i >> 1) & 3)
+                if constexpr (EC == 16) {
+                    // [32 rows][16 f32], 64-byte swizzle: 16-B chunk j of row i at j ^ ((i >> 1) & 3)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int js = j ^ ((lane >> 1) & 3);
-                    const uint32_t* v = &r[c][16 * hh + 4 * j];
-                    *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                    for (int j = 0; j < 4; ++j) {
+                        const int js = j ^ ((lane >> 1) & 3);
+                        const uint32_t* v = &r[c][16 * hh + 4 * j];
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + js * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                    }
+                } else {
+                    // [32 rows][8 f32], no swizzle
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t* v = &r[c][8 * hh + 4 * j];
+                        *reinterpret_cast<uint4*>(buf + lane * 32 + j * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_reduce_add_2d(&tm_c, buf, qc + 32 * c + 16 * hh, p0);
+                    tma_reduce_add_2d(&tm_c, buf, qc + 32 * c + EC * hh, p0);
                     bulk_commit_group();
                 }
                 ++nbuf;
@@ -811,7 +824,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
 // between MMAs.  Per SM a stage holds 32 KB of codes
 // for the same MMA work that needs 48 KB with 128 x 256 tiles on one SM: more
 // stages fit, and a third less data crosses from L2 per MMA.
-template <int KIND, int STAGES>
+template <int KIND, int STAGES, int EC = 16>
 struct PairCfg {
     static constexpr int G = KIND == KIND_F4 ? 2 : 1;  // scale groups per stage
     static constexpr int EPI_WARPS = 8;
@@ -826,7 +839,7 @@ struct PairCfg {
     static constexpr int SF_COL0 = 256;  // accumulator in columns [0, 256)
     static constexpr int SF_SLOTS_FIT = ((int)kTmemCols - SF_COL0) / SF_COLS_STAGE;
     static constexpr int SF_SLOTS = SF_SLOTS_FIT < STAGES ? SF_SLOTS_FIT : STAGES;
-    static constexpr int EPI_BUF = 32 * 16 * 4;
+    static constexpr int EPI_BUF = 32 * EC * 4;  // one 32 x EC staging box per epilogue warp
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -841,12 +854,12 @@ struct PairCfg {
     static_assert(STAGES <= 15, "one named barrier per stage");
 };
 
-template <int KIND, int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES>::THREADS, 1)
+template <int KIND, int STAGES, int EC = 16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES, EC>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                      const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    using C_ = PairCfg<KIND, STAGES>;
+    using C_ = PairCfg<KIND, STAGES, EC>;
     extern __shared__ uint8_t smem_raw[];
     // the same offsets in both CTAs: the MMAs and barrier addresses rely on it
     // aligned by an offset from the array itself: the compiler then keeps the
@@ -1108,7 +1121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tmem_empty_even);  // next tile's MMAs may start
-            epilogue_write_128(p, tm_c, r, p0, w.tq * 256 + h * 128, stage_buf, nbuf, lane);
+            epilogue_write_128<EC>(p, tm_c, r, p0, w.tq * 256 + h * 128, stage_buf, nbuf, lane);
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -1314,19 +1327,19 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 
 // CTA pairs that can be resident at once for a pair-kernel instantiation
 // (pairs need two SMs of one GPU processing cluster); cached per instantiation.
-template <int KIND, int STAGES>
+template <int KIND, int STAGES, int EC = 16>
 cudaError_t run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                      const CUtensorMap& tc, const GemmParams& p, int pairs, cudaStream_t st) {
-    using C_ = PairCfg<KIND, STAGES>;
-    auto kern = gemm_pair_kernel<KIND, STAGES>;
+    using C_ = PairCfg<KIND, STAGES, EC>;
+    auto kern = gemm_pair_kernel<KIND, STAGES, EC>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(2 * pairs), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
-template <int KIND, int STAGES>
+template <int KIND, int STAGES, int EC = 16>
 int pair_capacity() {
-    using C_ = PairCfg<KIND, STAGES>;
+    using C_ = PairCfg<KIND, STAGES, EC>;
     static std::mutex mu;
     static int cap[64];
     static bool known[64];
@@ -1337,7 +1350,7 @@ int pair_capacity() {
     }
     std::lock_guard<std::mutex> lock(mu);
     if (known[dev]) return cap[dev];
-    auto kern = gemm_pair_kernel<KIND, STAGES>;
+    auto kern = gemm_pair_kernel<KIND, STAGES, EC>;
     int n = 0;
     if (ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM) == cudaSuccess) {
         cudaLaunchConfig_t cfg;
@@ -1392,7 +1405,8 @@ int32_t band_rows(int32_t tiles_p, int64_t a_tile_bytes) {
 cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const uint8_t* x_sf, int x_fmt, int64_t P,
                         const void* y_codes, const uint8_t* y_sf, int y_fmt, int64_t Q, cudaStream_t st,
                         const char** detail) {
-    const int cap = kind == KIND_F4 ? pair_capacity<KIND_F4, 5>() : pair_capacity<KIND_F8F6F4, 6>();
+    // FP4: six stages fit when the epilogue stages 32 x 8 boxes (1 KB per warp)
+    const int cap = kind == KIND_F4 ? pair_capacity<KIND_F4, 6, 8>() : pair_capacity<KIND_F8F6F4, 6>();
     if (cap <= 0) return cudaErrorNotSupported;
     const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
     const int g = kind == KIND_F4 ? 2 : 1;
@@ -1422,7 +1436,8 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     auto opmap = p.op3d ? make_operand_map3 : make_operand_map;
     if (!opmap(&ta, x_codes, P, a.K, fk(x_fmt), 128) || !opmap(&tb, y_codes, Q, a.K, fk(y_fmt), 128) ||
         !make_sf_map(&tsa, x_sf, P, p.sf_groups, g, 1) || !make_sf_map(&tsb, y_sf, Q, p.sf_groups, g, 2) ||
-        (p.use_tma_epi && !make_c_map(&tc, a.C, a.M, a.N, 16, 32, 64))) {
+        (p.use_tma_epi && !(kind == KIND_F4 ? make_c_map(&tc, a.C, a.M, a.N, 8, 32, 0)
+                                            : make_c_map(&tc, a.C, a.M, a.N, 16, 32, 64)))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
         return cudaErrorInvalidValue;
     }
@@ -1437,7 +1452,7 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
         p.mode = 1;  // slices of (tile, stage) per pair
         pairs = (int)(p.total_units < cap ? p.total_units : cap);
     }
-    if (kind == KIND_F4) return run_pair<KIND_F4, 5>(ta, tb, tsa, tsb, tc, p, pairs, st);
+    if (kind == KIND_F4) return run_pair<KIND_F4, 6, 8>(ta, tb, tsa, tsb, tc, p, pairs, st);
     return run_pair<KIND_F8F6F4, 6>(ta, tb, tsa, tsb, tc, p, pairs, st);
 }
 
