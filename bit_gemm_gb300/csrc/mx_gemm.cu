@@ -824,18 +824,23 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
 // between MMAs.  Per SM a stage holds 32 KB of codes
 // for the same MMA work that needs 48 KB with 128 x 256 tiles on one SM: more
 // stages fit, and a third less data crosses from L2 per MMA.
-template <int KIND, int STAGES, int EC = 16>
+// SA: K atoms per stage (a stage is then one 3-D box of SA atoms per operand
+// and scale tensor: the per-stage issue cost is paid once per SA atoms).
+template <int KIND, int STAGES, int EC = 16, int SA = 1>
 struct PairCfg {
-    static constexpr int G = KIND == KIND_F4 ? 2 : 1;  // scale groups per stage
+    static constexpr int G = KIND == KIND_F4 ? 2 : 1;  // scale groups per atom
+    static constexpr int GS = SA * G;                   // scale groups per stage
     static constexpr int EPI_WARPS = 8;
     static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
     static constexpr int THREADS = 32 * (GATE_WARP + 1);
-    static constexpr int A_BYTES = 128 * kRowBytes;
-    static constexpr int B_BYTES = 128 * kRowBytes;
-    static constexpr int SFA_BYTES = G * 512;
-    static constexpr int SFB_BYTES = 2 * G * 512;
-    static constexpr int SF_COLS_A = 4 * G;
-    static constexpr int SF_COLS_STAGE = 12 * G;
+    static constexpr int A_ATOM = 128 * kRowBytes;
+    static constexpr int B_ATOM = 128 * kRowBytes;
+    static constexpr int A_BYTES = SA * A_ATOM;
+    static constexpr int B_BYTES = SA * B_ATOM;
+    static constexpr int SFA_BYTES = GS * 512;
+    static constexpr int SFB_BYTES = 2 * GS * 512;
+    static constexpr int SF_COLS_A = 4 * GS;
+    static constexpr int SF_COLS_STAGE = 12 * GS;
     static constexpr int SF_COL0 = 256;  // accumulator in columns [0, 256)
     static constexpr int SF_SLOTS_FIT = ((int)kTmemCols - SF_COL0) / SF_COLS_STAGE;
     static constexpr int SF_SLOTS = SF_SLOTS_FIT < STAGES ? SF_SLOTS_FIT : STAGES;
@@ -854,12 +859,12 @@ struct PairCfg {
     static_assert(STAGES <= 15, "one named barrier per stage");
 };
 
-template <int KIND, int STAGES, int EC = 16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES, EC>::THREADS, 1)
+template <int KIND, int STAGES, int EC = 16, int SA = 1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES, EC, SA>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                      const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    using C_ = PairCfg<KIND, STAGES, EC>;
+    using C_ = PairCfg<KIND, STAGES, EC, SA>;
     extern __shared__ uint8_t smem_raw[];
     // the same offsets in both CTAs: the MMAs and barrier addresses rely on it
     // aligned by an offset from the array itself: the compiler then keeps the
@@ -941,10 +946,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                 if (lane == 0 && rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.tx_a + p.tx_b + C_::SF_TX));
                 const uint32_t bar = full_even + (uint32_t)stage * 8;
                 const uint32_t dst = lbase + (uint32_t)stage * lstep;
-                // coordinates: operands (0, row, stage) in 3-D, (128 B * stage, row) in 2-D;
-                // scales (0, 4 G stage, 128-row tile)
-                const int32_t y = li == 0 ? a_row : li == 1 ? b_row : 4 * C_::G * kb;
-                const int32_t z = li < 2 ? kb : (li == 2 ? a_row >> 7 : w.tq * 2);
+                // coordinates: operands (0, row, first atom) in 3-D, (128 B * stage, row) in 2-D;
+                // scales (0, 4 GS stage, 128-row tile)
+                const int32_t y = li == 0 ? a_row : li == 1 ? b_row : 4 * C_::GS * kb;
+                const int32_t z = li < 2 ? SA * kb : (li == 2 ? a_row >> 7 : w.tq * 2);
                 if (p.op3d) {
                     if (lane < 4) tma_load_3d_pair_at(dst, lmap, 0, y, z, bar);
                 } else {
@@ -984,7 +989,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                 const uint32_t sf_id = KIND == KIND_F4 ? (uint32_t)(i & 1) * 2u : (uint32_t)i;
                 idesc[i] = p.idesc | (sf_id << 4) | (sf_id << 29);
             }
-            constexpr int k_elem_per_stage = KIND == KIND_F4 ? 256 : 128;
+            constexpr int k_elem_per_stage = SA * (KIND == KIND_F4 ? 256 : 128);
             constexpr int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
             int stage = 0;
             int sf_slot = 0;
@@ -1010,27 +1015,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                         const uint64_t sfa_desc = sfa_desc0 + stage * (C_::SFA_BYTES >> 4);
                         const uint64_t sfb_desc = sfb_desc0 + stage * (C_::SFB_BYTES >> 4);
                         // scale tiles -> TMEM: A group g at sf_col + 4g; B group g, row tile t
-                        // at sf_col + SF_COLS_A + 4 (2g + t)
+                        // at sf_col + SF_COLS_A + 4 (2g + t); g counts the stage's groups
+                        // (atom a holds groups a G ..)
 #pragma unroll
-                        for (int g = 0; g < C_::G; ++g) {
+                        for (int g = 0; g < C_::GS; ++g) {
                             tc_cp_pair_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
 #pragma unroll
                             for (int t = 0; t < 2; ++t)
                                 tc_cp_pair_32x128b_warpx4(sf_col + C_::SF_COLS_A + 4 * (2 * g + t),
-                                                          sfb_desc + (t * C_::G + g) * 32);
+                                                          sfb_desc + (t * C_::GS + g) * 32);
                         }
                         const int rem = p.K - kb * k_elem_per_stage;
-                        if (rem >= k_elem_per_stage) {
+                        if (SA > 1 || rem >= k_elem_per_stage) {
 #pragma unroll
-                            for (int i = 0; i < kMmaPerStage; ++i) {
-                                const int g = KIND == KIND_F4 ? (i >> 1) : 0;
-                                const uint32_t accum = (kb > w.kb0 || i > 0) ? 1u : 0u;
-                                if (KIND == KIND_F4)
-                                    mma_pair_mxf4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
-                                                  sf_col + C_::SF_COLS_A + 8 * g, accum);
-                                else
-                                    mma_pair_mxf8f6f4(tmem, a_desc + 2 * i, b_desc + 2 * i, idesc[i], sf_col + 4 * g,
+                            for (int a = 0; a < SA; ++a) {
+                                const uint64_t ad = a_desc + a * (C_::A_ATOM >> 4);
+                                const uint64_t bd = b_desc + a * (C_::B_ATOM >> 4);
+#pragma unroll
+                                for (int i = 0; i < kMmaPerStage; ++i) {
+                                    const int g = a * C_::G + (KIND == KIND_F4 ? (i >> 1) : 0);
+                                    const uint32_t accum = (kb > w.kb0 || a > 0 || i > 0) ? 1u : 0u;
+                                    if (KIND == KIND_F4)
+                                        mma_pair_mxf4(tmem, ad + 2 * i, bd + 2 * i, idesc[i], sf_col + 4 * g,
                                                       sf_col + C_::SF_COLS_A + 8 * g, accum);
+                                    else
+                                        mma_pair_mxf8f6f4(tmem, ad + 2 * i, bd + 2 * i, idesc[i], sf_col + 4 * g,
+                                                          sf_col + C_::SF_COLS_A + 8 * g, accum);
+                                }
                             }
                         } else {
                             // the ragged last stage of K
@@ -1327,19 +1338,19 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 
 // CTA pairs that can be resident at once for a pair-kernel instantiation
 // (pairs need two SMs of one GPU processing cluster); cached per instantiation.
-template <int KIND, int STAGES, int EC = 16>
+template <int KIND, int STAGES, int EC = 16, int SA = 1>
 cudaError_t run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                      const CUtensorMap& tc, const GemmParams& p, int pairs, cudaStream_t st) {
-    using C_ = PairCfg<KIND, STAGES, EC>;
-    auto kern = gemm_pair_kernel<KIND, STAGES, EC>;
+    using C_ = PairCfg<KIND, STAGES, EC, SA>;
+    auto kern = gemm_pair_kernel<KIND, STAGES, EC, SA>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(2 * pairs), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
-template <int KIND, int STAGES, int EC = 16>
+template <int KIND, int STAGES, int EC = 16, int SA = 1>
 int pair_capacity() {
-    using C_ = PairCfg<KIND, STAGES, EC>;
+    using C_ = PairCfg<KIND, STAGES, EC, SA>;
     static std::mutex mu;
     static int cap[64];
     static bool known[64];
@@ -1350,7 +1361,7 @@ int pair_capacity() {
     }
     std::lock_guard<std::mutex> lock(mu);
     if (known[dev]) return cap[dev];
-    auto kern = gemm_pair_kernel<KIND, STAGES, EC>;
+    auto kern = gemm_pair_kernel<KIND, STAGES, EC, SA>;
     int n = 0;
     if (ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM) == cudaSuccess) {
         cudaLaunchConfig_t cfg;
@@ -1405,11 +1416,17 @@ int32_t band_rows(int32_t tiles_p, int64_t a_tile_bytes) {
 cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const uint8_t* x_sf, int x_fmt, int64_t P,
                         const void* y_codes, const uint8_t* y_sf, int y_fmt, int64_t Q, cudaStream_t st,
                         const char** detail) {
-    // FP4: six stages fit when the epilogue stages 32 x 8 boxes (1 KB per warp)
-    const int cap = kind == KIND_F4 ? pair_capacity<KIND_F4, 6, 8>() : pair_capacity<KIND_F8F6F4, 6>();
+    // Two K atoms per stage when K allows (one 3-D box per operand and scale
+    // tensor per two atoms: the per-stage issue cost is halved); three such
+    // stages hold what six single-atom ones did.  FP4 stages its epilogue
+    // through 32 x 8 boxes (1 KB per warp) to make room.
+    const int64_t k_atom = kind == KIND_F4 ? 256 : 128;
+    const int sa = (a.K % (2 * k_atom)) == 0 ? 2 : 1;
+    const int cap = kind == KIND_F4 ? (sa == 2 ? pair_capacity<KIND_F4, 3, 8, 2>() : pair_capacity<KIND_F4, 6, 8>())
+                                    : (sa == 2 ? pair_capacity<KIND_F8F6F4, 3, 16, 2>() : pair_capacity<KIND_F8F6F4, 6>());
     if (cap <= 0) return cudaErrorNotSupported;
-    const int64_t k_per_stage = kind == KIND_F4 ? 256 : 128;
-    const int g = kind == KIND_F4 ? 2 : 1;
+    const int64_t k_per_stage = sa * k_atom;
+    const int g = sa * (kind == KIND_F4 ? 2 : 1);
     auto fk = [&](int f) { return f == FMT_E4M3 ? 0 : (kind == KIND_F4 ? 1 : 2); };
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -1427,14 +1444,17 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     p.ldc = a.N;
     p.sfa = x_sf;
     p.sfb = y_sf;
-    p.tx_a = 128u * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
-    p.tx_b = 128u * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.tx_a = (uint32_t)(sa * 128) * (fk(x_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
+    p.tx_b = (uint32_t)(sa * 128) * (fk(y_fmt) == 2 ? kRowBytes / 2 : kRowBytes);
     p.nb = (int32_t)(a.K / 32);
     CUtensorMap ta, tb, tsa, tsb, tc;
     std::memset(&tc, 0, sizeof(tc));
-    p.op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
-    auto opmap = p.op3d ? make_operand_map3 : make_operand_map;
-    if (!opmap(&ta, x_codes, P, a.K, fk(x_fmt), 128) || !opmap(&tb, y_codes, Q, a.K, fk(y_fmt), 128) ||
+    p.op3d = (a.K % k_atom) == 0 ? 1 : 0;
+    auto opmap = [&](CUtensorMap* m, const void* codes, int64_t rows, int f) {
+        return p.op3d ? make_operand_map3n(m, codes, rows, a.K, fk(f), 128, sa)
+                      : make_operand_map(m, codes, rows, a.K, fk(f), 128);
+    };
+    if (!opmap(&ta, x_codes, P, x_fmt) || !opmap(&tb, y_codes, Q, y_fmt) ||
         !make_sf_map(&tsa, x_sf, P, p.sf_groups, g, 1) || !make_sf_map(&tsb, y_sf, Q, p.sf_groups, g, 2) ||
         (p.use_tma_epi && !(kind == KIND_F4 ? make_c_map(&tc, a.C, a.M, a.N, 8, 32, 0)
                                             : make_c_map(&tc, a.C, a.M, a.N, 16, 32, 64)))) {
@@ -1451,6 +1471,10 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     } else {
         p.mode = 1;  // slices of (tile, stage) per pair
         pairs = (int)(p.total_units < cap ? p.total_units : cap);
+    }
+    if (sa == 2) {
+        if (kind == KIND_F4) return run_pair<KIND_F4, 3, 8, 2>(ta, tb, tsa, tsb, tc, p, pairs, st);
+        return run_pair<KIND_F8F6F4, 3, 16, 2>(ta, tb, tsa, tsb, tc, p, pairs, st);
     }
     if (kind == KIND_F4) return run_pair<KIND_F4, 6, 8>(ta, tb, tsa, tsb, tc, p, pairs, st);
     return run_pair<KIND_F8F6F4, 6>(ta, tb, tsa, tsb, tc, p, pairs, st);
