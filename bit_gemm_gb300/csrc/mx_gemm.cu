@@ -69,7 +69,8 @@ struct GemmParams {
     int32_t tiles_p, tiles_q;
     int32_t k_stages;      // stages of 128 bytes of K
     int32_t sf_groups;     // 4-block scale groups per 128-row scale tile (NB4 / 4)
-    int32_t mode;          // 0 = whole tiles round-robin, 1 = equal slices of (tile, stage)
+    int32_t mode;          // 0 = whole tiles round-robin, 1 = equal slices of (tile, stage),
+                           // 2 = whole tiles for the full rounds, the remaining tiles as in 1
     int64_t total_units;   // tiles * k_stages
     uint64_t wait_limit_ns;
     uint32_t idesc;        // instruction descriptor without scale-factor ids
@@ -98,6 +99,18 @@ struct Work {
 
 // The iter-th unit of work of worker `id` of `count` (a CTA, or a CTA pair);
 // identical in every role.
+// Tile index -> (row tile, column tile) in bands of group_p row tiles: within
+// a band the row tile varies fastest, so the band's A rows stay in L2 while
+// its column tiles stream past.
+__device__ __forceinline__ void banded_tile(const GemmParams& p, int64_t tile, Work& w) {
+    const int64_t band_tiles = (int64_t)p.group_p * p.tiles_q;
+    const int64_t band = tile / band_tiles;
+    const int64_t r = tile - band * band_tiles;
+    const int64_t rows_in_band = min((int64_t)p.group_p, (int64_t)p.tiles_p - band * p.group_p);
+    w.tp = (int32_t)(band * p.group_p + r % rows_in_band);
+    w.tq = (int32_t)(r / rows_in_band);
+}
+
 __device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint32_t count, int iter, Work& w) {
     const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
     int64_t tile;
@@ -106,14 +119,32 @@ __device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint3
         if (tile >= tiles) return false;
         w.kb0 = 0;
         w.kb1 = p.k_stages;
-        // bands of group_p row tiles: within a band the row tile varies fastest,
-        // so the band's A rows stay in L2 while its column tiles stream past
-        const int64_t band_tiles = (int64_t)p.group_p * p.tiles_q;
-        const int64_t band = tile / band_tiles;
-        const int64_t r = tile - band * band_tiles;
-        const int64_t rows_in_band = min((int64_t)p.group_p, (int64_t)p.tiles_p - band * p.group_p);
-        w.tp = (int32_t)(band * p.group_p + r % rows_in_band);
-        w.tq = (int32_t)(r / rows_in_band);
+        banded_tile(p, tile, w);
+        return true;
+    } else if (p.mode == 2) {
+        // every worker takes `rounds` whole tiles; the tiles left over (fewer
+        // than the workers) are cut into equal slices of (tile, stage), so no
+        // worker idles through a last partial round
+        const int64_t rounds = tiles / count;
+        if (iter < rounds) {
+            tile = (int64_t)id + (int64_t)iter * count;
+            w.kb0 = 0;
+            w.kb1 = p.k_stages;
+            banded_tile(p, tile, w);
+            return true;
+        }
+        const int64_t first = rounds * count;
+        const int64_t units = (tiles - first) * p.k_stages;
+        const int64_t u0 = units * id / count;
+        const int64_t u1 = units * (id + 1) / count;
+        if (u0 >= u1) return false;
+        const int64_t t = u0 / p.k_stages + (iter - rounds);
+        const int64_t b = t * p.k_stages > u0 ? t * p.k_stages : u0;
+        const int64_t e = (t + 1) * p.k_stages < u1 ? (t + 1) * p.k_stages : u1;
+        if (b >= e) return false;
+        w.kb0 = (int32_t)(b - t * p.k_stages);
+        w.kb1 = (int32_t)(e - t * p.k_stages);
+        banded_tile(p, first + t, w);
         return true;
     } else {
         const int64_t u0 = p.total_units * id / count;
@@ -1466,7 +1497,8 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     p.group_p = band_rows(p.tiles_p, 256 * (x_fmt == FMT_E2M1 ? a.K / 2 : a.K));
     int pairs;
     if (tiles >= cap || p.k_stages < 4) {
-        p.mode = 0;
+        // whole tiles; a last partial round is split along K over all pairs
+        p.mode = (tiles > cap && tiles % cap != 0 && p.k_stages >= 4) ? 2 : 0;
         pairs = (int)(tiles < cap ? tiles : cap);
     } else {
         p.mode = 1;  // slices of (tile, stage) per pair
