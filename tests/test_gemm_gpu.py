@@ -149,6 +149,20 @@ def test_pair_tiles(M, N, K, fa, fb):
     run_full(randn(rng, (M, K)), randn(rng, (N, K)), fa, fb, randn(rng, (M, N)))
 
 
+# ---------------------------------------- two K atoms per pipeline stage
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (32, 1000, 512, mx.E4M3FN, mx.E2M1),     # decode-shaped, MMA N = 32, mixed formats
+    (5, 1300, 1024, mx.E2M1, mx.E2M1),       # decode-shaped, packed FP4 atoms of 256 elements
+    (17, 2052, 768, mx.E4M3FN, mx.E4M3FN),   # MMA N = 32 with 17 real rows, ragged weight tiles
+    (16, 1030, 512, mx.E4M3FN, mx.E4M3FN),   # N % 4 != 0: the per-element epilogue
+    (2560, 2048, 1024, mx.E4M3FN, mx.E4M3FN),  # pairs: 80 tiles on 76 pairs, the last 4 split along K
+])
+def test_two_atom_stages(M, N, K, fa, fb):
+    rng = np.random.default_rng(M * 3 + N + K)
+    run_full(randn(rng, (M, K)), randn(rng, (N, K)), fa, fb, randn(rng, (M, N)))
+
+
 # ------------------------------------------------------ row-major scales
 
 @pytest.mark.parametrize("M,N,K,fa,fb", [
