@@ -182,8 +182,13 @@ struct Cfg {
     // the next tile's MMAs overlap the write-out of this one
     static constexpr int ACC = (!SWAP && 2 * BN <= 256) ? 2 : 1;
     static constexpr int EPI_WARPS = (!SWAP && BN == 256) ? 8 : 4;
-    static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
-    static constexpr int THREADS = 32 * (GATE_WARP + 1);
+    static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp(s)
+    // MMA-issuing warps: with several atoms per stage (decode shapes, where one
+    // thread's issue rate sets the pace) each of MW warps takes SA / MW atoms
+    // of every stage into its own accumulator; the epilogue adds them.  Warp 1
+    // and, for MW = 2, the warp after the gate.
+    static constexpr int MW = (SWAP && SA == 2 && !ACT) ? 2 : 1;
+    static constexpr int THREADS = 32 * (GATE_WARP + MW);
     static constexpr int A_ATOM = kBlockM * kRowBytes;                // 16 KB
     static constexpr int B_ATOM = BN * kRowBytes;
     static constexpr int A_BYTES = SA * A_ATOM;
@@ -221,7 +226,8 @@ struct Cfg {
     static_assert(STAGES <= (ACT ? 14 : 15), "named barriers 1..STAGES (and 15 for the activation prologue)");
     static_assert(SF_SLOTS >= 2, "at least two scale slots in TMEM");
     static_assert(SF_COL0 + SF_SLOTS * SF_COLS_STAGE <= (int)kTmemCols, "TMEM columns");
-    static_assert(ACC * BN <= SF_COL0, "accumulator columns");
+    static_assert(ACC * MW * BN <= SF_COL0, "accumulator columns");
+    static_assert(SA % MW == 0, "whole atoms per MMA warp");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -326,13 +332,13 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         for (int s = 0; s < STAGES; ++s) {
             // row-major scales: the 32 producer lanes' cp.async arrivals as well
             mbar_init(&full[s], p.sf_rowmajor ? 33 : 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], C_::MW);  // one commit per MMA warp
         }
         for (int a = 0; a < ACC; ++a) {
-            mbar_init(&tmem_full[a], 1);
+            mbar_init(&tmem_full[a], C_::MW);
             mbar_init(&tmem_empty[a], C_::EPI_WARPS);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, C_::MW);
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_a);
@@ -568,11 +574,12 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, p.wait_limit_ns, err);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (C_::MW > 1 && warp == C_::GATE_WARP + 1)) {
         // ---------------------------------------------------------- MMA issue
         // The whole warp walks the schedule and syncs on stage s's named
         // barrier (1 + s) with the gate warp, which has seen the stage's data
-        // land; lane 0 issues.  After an abort the warp keeps walking (and
+        // land; lane 0 issues.  MMA warp m (of MW) issues atoms
+        // [m SA / MW, (m + 1) SA / MW) of every stage into accumulator m.  After an abort the warp keeps walking (and
         // syncing) without issuing, so its syncs and the gate's always pair up.
         // Everything that does not depend on the stage is built once: the
         // shared-memory descriptors of stage 0 (a stage's descriptors differ
@@ -592,6 +599,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         }
         constexpr int k_elem_per_stage = SA * (KIND == KIND_F4 ? 256 : 128);
         constexpr int k_elem_per_mma = KIND == KIND_F4 ? 64 : 32;
+        constexpr int AW = SA / C_::MW;  // atoms per MMA warp
+        const int m = warp == 1 ? 0 : 1;
+        const int a_first = m * AW;
         int stage = 0;
         int sf_slot = 0;
         bool live = true;  // false after an abort: walk without issuing
@@ -607,9 +617,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 live = false;
                 if (lane == 0) *abort_flag = 1;
             }
-            const uint32_t d_tmem = tmem + kAccCol + acc * BN;
+            const uint32_t d_tmem = tmem + kAccCol + (acc * C_::MW + m) * BN;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                named_bar_sync(1 + stage, 64);  // the gate saw this stage's data land
+                named_bar_sync(1 + stage, 32 * (1 + C_::MW));  // the gate saw this stage's data land
                 if (lane == 0 && live) {
                     tc_fence_after();
                     // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
@@ -632,7 +642,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                         // SFB group g, row-tile t at sf_col + SF_COLS_A + 4(g*SFB_TILES + t)
                         // (g counts the stage's groups: atom a holds groups a*G ..)
 #pragma unroll
-                        for (int g = 0; g < C_::GS; ++g) {
+                        for (int gg = 0; gg < AW * C_::G; ++gg) {
+                            const int g = a_first * C_::G + gg;  // this warp's atoms' groups
                             tc_cp_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
 #pragma unroll
                             for (int t = 0; t < C_::SFB_TILES; ++t)
@@ -640,14 +651,15 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                                                      sfb_desc + (t * C_::GS + g) * 32);
                         }
 #pragma unroll
-                        for (int a = 0; a < SA; ++a) {
+                        for (int aa = 0; aa < AW; ++aa) {
+                            const int a = a_first + aa;
                             // atom a of the stage: its A and B rows follow the previous atom's
                             const uint64_t ad = a_desc + a * (C_::A_ATOM >> 4);
                             const uint64_t bd = b_desc + a * (C_::B_ATOM >> 4);
 #pragma unroll
                             for (int i = 0; i < kMmaPerStage; ++i) {
                                 const int g = a * C_::G + (KIND == KIND_F4 ? (i >> 1) : 0);
-                                const uint32_t accum = (kb > w.kb0 || a > 0 || i > 0) ? 1u : 0u;
+                                const uint32_t accum = (kb > w.kb0 || aa > 0 || i > 0) ? 1u : 0u;
                                 if (KIND == KIND_F4)
                                     mma_mxf4(d_tmem, ad + 2 * i, bd + 2 * i, idesc[i], sf_col + 4 * g,
                                              sf_col + C_::SF_COLS_A + 4 * g * C_::SFB_TILES, accum);
@@ -715,7 +727,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                         if (lane == 0) *abort_flag = 1;
                     }
                 }
-                named_bar_sync(1 + stage, 64);
+                named_bar_sync(1 + stage, 32 * (1 + C_::MW));
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -740,7 +752,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             tc_fence_after();
             const int32_t p0 = w.tp * kBlockM + 32 * q;  // first MMA-A row of this warp
             const int32_t q0 = w.tq * BN;
-            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + kAccCol + acc * BN;
+            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + kAccCol + acc * C_::MW * BN;
             if constexpr (C_::EPI_WARPS == 8) {
                 // this warp: rows p0..p0+31, columns h*128 .. h*128+127 of the tile
                 const int h = (warp - 2) >> 2;
@@ -754,15 +766,23 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 epilogue_write_128(p, tm_c, r, p0, q0 + h * 128, stage_buf, nbuf, lane);
             } else if (SWAP) {
                 // lane i holds acc(p0 + i, q0 + j), j < BN  ->  C[q0 + j][p0 + i]
-                uint32_t r[BN];
+                // (MW accumulators: their sum)
+                uint32_t r[C_::MW][BN];
 #pragma unroll
-                for (int c = 0; c < BN / 16; ++c) {
-                    uint32_t t[16];
-                    tmem_ld_32x32b_x16(t_row + 16 * c, t);
+                for (int mm = 0; mm < C_::MW; ++mm)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r[16 * c + j] = t[j];
-                }
+                    for (int c = 0; c < BN / 16; ++c) {
+                        uint32_t t[16];
+                        tmem_ld_32x32b_x16(t_row + mm * BN + 16 * c, t);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) r[mm][16 * c + j] = t[j];
+                    }
                 tmem_ld_wait();
+#pragma unroll
+                for (int mm = 1; mm < C_::MW; ++mm)
+#pragma unroll
+                    for (int j = 0; j < BN; ++j)
+                        r[0][j] = __float_as_uint(__uint_as_float(r[0][j]) + __uint_as_float(r[mm][j]));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tmem_empty[acc]);
@@ -772,7 +792,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     __syncwarp();
                     float* f = reinterpret_cast<float*>(buf);
 #pragma unroll
-                    for (int j = 0; j < BN; ++j) f[j * 32 + lane] = __uint_as_float(r[j]);  // [BN rows][32 cols]
+                    for (int j = 0; j < BN; ++j) f[j * 32 + lane] = __uint_as_float(r[0][j]);  // [BN rows][32 cols]
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -785,7 +805,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     if (pr < p.P) {
 #pragma unroll
                         for (int j = 0; j < BN; ++j)
-                            if (q0 + j < p.Q) atomicAdd(p.C + (int64_t)(q0 + j) * p.ldc + pr, __uint_as_float(r[j]));
+                            if (q0 + j < p.Q) atomicAdd(p.C + (int64_t)(q0 + j) * p.ldc + pr, __uint_as_float(r[0][j]));
                     }
                 }
             } else {
