@@ -8,19 +8,27 @@
 // hardware (kind::mxf8f6f4: K = 32 per instruction, one scale per row;
 // kind::mxf4: K = 64 per instruction, two scales per row).
 //
-// Kernel shape (one CTA per SM, 192 threads):
+// Two kernels, both persistent (one CTA, or one CTA pair, per SM or SM pair):
+//   gemm_kernel       one CTA per 128 x BN tile: M or N <= 128, row-major
+//                     scales, and the swapped decode shapes;
+//   gemm_pair_kernel  256 x 256 tiles on a CTA pair (tcgen05 .cta_group::2).
+// Roles in a CTA:
 //   warp 0      TMA producer: A/B code tiles (128-byte swizzled, K-major) and
 //               the 512-byte scale tiles into a STAGES-deep shared-memory ring.
 //   warp 1      allocates TMEM; one lane copies the scale tiles to TMEM
-//               (tcgen05.cp) and issues the MMAs into an f32 TMEM accumulator.
-//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging ->
+//               (tcgen05.cp) and issues the MMAs into an f32 TMEM accumulator
+//               (decode shapes: a second MMA warp takes every stage's second
+//               K atom into a second accumulator).
+//   gate warp   waits on each stage's barrier and passes it to the MMA warp(s)
+//               through a named barrier, so the issuing thread never touches
+//               shared memory between MMAs.
+//   epilogue    4 or 8 warps: TMEM -> registers -> swizzled shared staging ->
 //               TMA reduce-add into C (C += acc, performed at L2), so C is read
 //               and written in place with no extra pass.
-// Work is either whole 128 x BN tiles handed out round-robin (large shapes),
-// or equal slices of the (tile, k-stage) space per CTA (few-tile shapes such
-// as decode; partial sums meet in C through the same reduce-add).  For M <= 64
-// the operands are swapped (C^T = Bt * A^T) so the long N side fills the
-// 128-row MMA dimension.
+// The work schedule (whole tiles, or equal slices of the (tile, K stage)
+// space, whose partial sums meet in C through the same reduce-add) is in
+// mx_schedule.h.  For M <= 64 the operands are swapped (C^T = Bt * A^T) so the
+// long N side fills the 128-row MMA dimension.
 //
 // Every mbarrier wait is bounded (see mx_device.cuh); a CTA that gives up sets
 // the device error word, drains what it issued, frees its TMEM and exits.
@@ -35,6 +43,7 @@
 #include "mx_device.cuh"
 #include "mx_internal.h"
 #include "mx_quant_block.cuh"
+#include "mx_schedule.h"
 
 namespace mx {
 
@@ -93,75 +102,6 @@ struct GemmParams {
     int32_t act_bf16;      // 1: bf16, 0: f32
 };
 
-struct Work {
-    int32_t tp, tq, kb0, kb1;
-};
-
-// The iter-th unit of work of worker `id` of `count` (a CTA, or a CTA pair);
-// identical in every role.
-// Tile index -> (row tile, column tile) in bands of group_p row tiles: within
-// a band the row tile varies fastest, so the band's A rows stay in L2 while
-// its column tiles stream past.
-__device__ __forceinline__ void banded_tile(const GemmParams& p, int64_t tile, Work& w) {
-    const int64_t band_tiles = (int64_t)p.group_p * p.tiles_q;
-    const int64_t band = tile / band_tiles;
-    const int64_t r = tile - band * band_tiles;
-    const int64_t rows_in_band = min((int64_t)p.group_p, (int64_t)p.tiles_p - band * p.group_p);
-    w.tp = (int32_t)(band * p.group_p + r % rows_in_band);
-    w.tq = (int32_t)(r / rows_in_band);
-}
-
-__device__ __forceinline__ bool get_work(const GemmParams& p, uint32_t id, uint32_t count, int iter, Work& w) {
-    const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
-    int64_t tile;
-    if (p.mode == 0) {
-        tile = (int64_t)id + (int64_t)iter * count;
-        if (tile >= tiles) return false;
-        w.kb0 = 0;
-        w.kb1 = p.k_stages;
-        banded_tile(p, tile, w);
-        return true;
-    } else if (p.mode == 2) {
-        // every worker takes `rounds` whole tiles; the tiles left over (fewer
-        // than the workers) are cut into equal slices of (tile, stage), so no
-        // worker idles through a last partial round
-        const int64_t rounds = tiles / count;
-        if (iter < rounds) {
-            tile = (int64_t)id + (int64_t)iter * count;
-            w.kb0 = 0;
-            w.kb1 = p.k_stages;
-            banded_tile(p, tile, w);
-            return true;
-        }
-        const int64_t first = rounds * count;
-        const int64_t units = (tiles - first) * p.k_stages;
-        const int64_t u0 = units * id / count;
-        const int64_t u1 = units * (id + 1) / count;
-        if (u0 >= u1) return false;
-        const int64_t t = u0 / p.k_stages + (iter - rounds);
-        const int64_t b = t * p.k_stages > u0 ? t * p.k_stages : u0;
-        const int64_t e = (t + 1) * p.k_stages < u1 ? (t + 1) * p.k_stages : u1;
-        if (b >= e) return false;
-        w.kb0 = (int32_t)(b - t * p.k_stages);
-        w.kb1 = (int32_t)(e - t * p.k_stages);
-        banded_tile(p, first + t, w);
-        return true;
-    } else {
-        const int64_t u0 = p.total_units * id / count;
-        const int64_t u1 = p.total_units * (id + 1) / count;
-        if (u0 >= u1) return false;
-        tile = u0 / p.k_stages + iter;
-        const int64_t b = tile * p.k_stages > u0 ? tile * p.k_stages : u0;
-        const int64_t e = (tile + 1) * p.k_stages < u1 ? (tile + 1) * p.k_stages : u1;
-        if (b >= e) return false;
-        w.kb0 = (int32_t)(b - tile * p.k_stages);
-        w.kb1 = (int32_t)(e - tile * p.k_stages);
-    }
-    w.tp = (int32_t)(tile % p.tiles_p);
-    w.tq = (int32_t)(tile / p.tiles_p);
-    return true;
-}
-
 template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0, int SA = 1>
 struct Cfg {
     // SA: K atoms (128 bytes of K per operand row) per pipeline stage; a stage
@@ -187,7 +127,8 @@ struct Cfg {
     // thread's issue rate sets the pace) each of MW warps takes SA / MW atoms
     // of every stage into its own accumulator; the epilogue adds them.  Warp 1
     // and, for MW = 2, the warp after the gate.
-    static constexpr int MW = (SWAP && SA == 2 && !ACT) ? 2 : 1;
+    static constexpr int MW = (SWAP && SA == 2) ? 2 : 1;
+    static constexpr int PRO_WARPS = GATE_WARP + MW - 1;  // warps 1.. that quantize resident activations
     static constexpr int THREADS = 32 * (GATE_WARP + MW);
     static constexpr int A_ATOM = kBlockM * kRowBytes;                // 16 KB
     static constexpr int B_ATOM = BN * kRowBytes;
@@ -370,7 +311,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             kb_hi = max(kb_hi, w.kb1);
         }
         if (kb_hi <= kb_lo) kb_lo = kb_hi = 0;
-        if (warp >= 1 && warp <= C_::GATE_WARP) {
+        if (warp >= 1 && warp <= C_::PRO_WARPS) {
             // ------------------------------------------------ activation prologue
             // The warps that are idle while the producer starts streaming the
             // weights quantize this CTA's K stages of the activations once, with
@@ -379,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             // Rows past M and elements past K become zero codes.
             constexpr int BPA = KIND == KIND_F4 ? 8 : 4;  // 32-element blocks per atom
             constexpr int AFMT = KIND == KIND_F4 ? FMT_E2M1 : FMT_E4M3;
-            const int nthr = 32 * C_::GATE_WARP;
+            const int nthr = 32 * C_::PRO_WARPS;
             const int64_t items = (int64_t)SA * (kb_hi - kb_lo) * BN * BPA;
             // block i: atom a (of the CTA's range), row r, block j of the atom; its first element k
             auto item = [&](int64_t i, int& a, int& r, int& j, int64_t& k) {
@@ -476,7 +417,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             }
             fence_proxy_async_smem();  // generic writes, read by the tensor core
             __syncwarp();
-            named_bar_sync(15, 32 * C_::GATE_WARP);
+            named_bar_sync(15, 32 * C_::PRO_WARPS);
         }
     }
 
