@@ -298,6 +298,24 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The first two work units, computed before the wait (the integer
+    // divisions of the schedule take a few hundred ns of one warp's time,
+    // which then overlap the previous kernel's tail instead of delaying the
+    // first load and the MMA warps' first tile change).
+    Work wl0, wl1;
+    const bool hl0 = get_work(p, blockIdx.x, gridDim.x, 0, wl0);
+    const bool hl1 = hl0 && get_work(p, blockIdx.x, gridDim.x, 1, wl1);
+    auto work_at = [&](int it, Work& w) -> bool {
+        if (it == 0) {
+            w = wl0;
+            return hl0;
+        }
+        if (it == 1) {
+            w = wl1;
+            return hl1;
+        }
+        return get_work(p, blockIdx.x, gridDim.x, it, w);
+    };
     // set-up above overlaps the previous kernel's tail; global memory from here on
     pdl_wait();
 
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
     int kb_lo = 0x7FFFFFFF, kb_hi = 0;
     if constexpr (C_::ACT) {
         Work w;
-        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+        for (int it = 0; work_at(it, w); ++it) {
             kb_lo = min(kb_lo, w.kb0);
             kb_hi = max(kb_hi, w.kb1);
         }
@@ -436,10 +454,11 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                                                   : li == 2 ? C_::OFF_SFA : C_::OFF_SFB);
         const uint32_t lstep = li == 0 ? C_::A_BYTES : li == 1 ? C_::B_BYTES : li == 2 ? C_::SFA_BYTES : C_::SFB_BYTES;
         uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
+        int fills = 0;
         uint32_t issued_phase = 0;
         bool ok = true;
         Work w;
-        for (int it = 0; ok && get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+        for (int it = 0; ok && work_at(it, w); ++it) {
             const int32_t p0 = w.tp * kBlockM;
             const int32_t q0 = w.tq * BN;
             const int nk = w.kb1 - w.kb0;
@@ -448,7 +467,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // (the abort flag is consulted only when a bounded wait gives up:
                 // a shared-memory load and branch per stage would delay issue)
                 int okw = 1;
-                if (lane == 0) okw = mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
+                // (the first STAGES fills find their slots free: no wait)
+                if (lane == 0 && fills >= STAGES) okw = mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
+                ++fills;
                 okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
                 if (!okw) {
                     if (lane == 0) *abort_flag = 1;
@@ -547,7 +568,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         int sf_slot = 0;
         bool live = true;  // false after an abort: walk without issuing
         Work w;
-        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+        for (int it = 0; work_at(it, w); ++it) {
             const int acc = it % ACC;
             const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
             int okt = 1;
@@ -657,7 +678,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         uint32_t phase = 0;
         bool live = true;
         Work w;
-        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+        for (int it = 0; work_at(it, w); ++it) {
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (live) {
                     int okw = 1;
@@ -682,7 +703,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         (void)stage_buf;
         int nbuf = 0;  // chunks issued so far by this warp (buffer = nbuf % NBUF)
         Work w;
-        for (int it = 0; get_work(p, blockIdx.x, gridDim.x, it, w); ++it) {
+        for (int it = 0; work_at(it, w); ++it) {
             const int acc = it % ACC;
             const uint32_t acc_phase = (uint32_t)(it / ACC) & 1u;
             bool ok = !*abort_flag && mbar_wait(&tmem_full[acc], acc_phase, p.wait_limit_ns, err);
