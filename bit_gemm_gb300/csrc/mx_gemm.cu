@@ -39,6 +39,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
@@ -72,6 +73,7 @@ constexpr int kRowBytes = 128;        // bytes of K per tile row per stage (one 
 constexpr int kMmaPerStage = 4;       // 4 MMAs of 32 bytes of K each
 constexpr int kAccCol = 0;            // accumulator buffers at columns [0, ACC * BN)
 constexpr uint32_t kTmemCols = 512;
+constexpr int kActStreamed = -1;      // ACT_ATOMS value: activations quantized stage by stage
 
 struct GemmParams {
     int32_t P, Q, K;       // rows of the MMA A operand, rows of the MMA B operand, reduction length
@@ -109,8 +111,11 @@ struct Cfg {
     // per-stage costs (barrier round trips, load issue) are paid once per SA
     // atoms.  SA > 1 needs K a whole number of stages and tensor-core scales.
     // ACT_ATOMS > 0: the activations (the MMA B operand of a swapped shape) are
-    // quantized by the kernel into a resident region of that many K stages
+    // quantized by the kernel into a resident region of that many K stages.
+    // ACT_ATOMS == kActStreamed: they are quantized stage by stage into the
+    // ring's B slots by ACT_WARPS warps of their own, as the weights stream.
     static constexpr bool ACT = ACT_ATOMS > 0;
+    static constexpr bool SACT = ACT_ATOMS == kActStreamed;
     static constexpr int G = KIND == KIND_F4 ? 2 : 1;                 // scale groups per atom
     static constexpr int GS = SA * G;                                  // scale groups per stage
     // 128-row scale tiles covering the BN rows of a B tile (tiles start on
@@ -129,14 +134,17 @@ struct Cfg {
     // and, for MW = 2, the warp after the gate.
     static constexpr int MW = (SWAP && SA == 2) ? 2 : 1;
     static constexpr int PRO_WARPS = GATE_WARP + MW - 1;  // warps 1.. that quantize resident activations
-    static constexpr int THREADS = 32 * (GATE_WARP + MW);
+    static constexpr int ACT_WARP0 = GATE_WARP + MW;      // streamed activations: the last ACT_WARPS warps
+    static constexpr int ACT_WARPS = SACT ? 4 : 0;
+    static constexpr int THREADS = 32 * (GATE_WARP + MW + ACT_WARPS);
     static constexpr int A_ATOM = kBlockM * kRowBytes;                // 16 KB
     static constexpr int B_ATOM = BN * kRowBytes;
     static constexpr int A_BYTES = SA * A_ATOM;
     static constexpr int B_BYTES = ACT ? 0 : SA * B_ATOM;
     static constexpr int SFA_BYTES = GS * 512;
     static constexpr int SFB_BYTES = ACT ? 0 : GS * SFB_TILES * 512;
-    static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);  // full scale boxes of a stage
+    // full scale boxes of a stage that TMA loads (streamed activations: A's only)
+    static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + (SACT ? 0 : SFB_BYTES));
     static constexpr int ACT_BYTES = BN * kRowBytes;  // one resident K stage of the activations
     static constexpr int ACT_SF_BYTES = G * 512;
     static constexpr int SF_COLS_A = 4 * GS;
@@ -158,8 +166,9 @@ struct Cfg {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_ACT = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
-    static constexpr int OFF_ACT_SF = OFF_ACT + ACT_ATOMS * ACT_BYTES;
-    static constexpr int OFF_EPI = (OFF_ACT_SF + ACT_ATOMS * ACT_SF_BYTES + 1023) / 1024 * 1024;
+    static constexpr int RES_ATOMS = ACT ? ACT_ATOMS : 0;  // resident activation stages
+    static constexpr int OFF_ACT_SF = OFF_ACT + RES_ATOMS * ACT_BYTES;
+    static constexpr int OFF_EPI = (OFF_ACT_SF + RES_ATOMS * ACT_SF_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * NBUF * EPI_BUF;
     static constexpr int BAR_BYTES = (2 * STAGES + 2 * ACC + 1) * 8 + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;           // + alignment slack
@@ -169,6 +178,13 @@ struct Cfg {
     static_assert(SF_COL0 + SF_SLOTS * SF_COLS_STAGE <= (int)kTmemCols, "TMEM columns");
     static_assert(ACC * MW * BN <= SF_COL0, "accumulator columns");
     static_assert(SA % MW == 0, "whole atoms per MMA warp");
+    static_assert(!SACT || (SWAP && BN == 16), "streamed activations: swapped shapes, up to 16 rows");
+    // An activation warp waits for fill n's slot by the parity of the slot's
+    // empty barrier, which is unambiguous only while the barrier is at most
+    // one phase behind: its previous wait (fill n - ACT_WARPS) guarantees fill
+    // n - ACT_WARPS - STAGES was consumed, and fill n needs n - 2 STAGES, so
+    // ACT_WARPS may not exceed STAGES.
+    static_assert(ACT_WARPS <= STAGES, "activation warps at most one ring phase ahead");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -272,7 +288,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             // row-major scales: the 32 producer lanes' cp.async arrivals as well
-            mbar_init(&full[s], p.sf_rowmajor ? 33 : 1);
+            // + the activation warp that fills the stage's B slot, when streamed
+            mbar_init(&full[s], p.sf_rowmajor ? 33 : (C_::SACT ? 2 : 1));
             mbar_init(&empty[s], C_::MW);  // one commit per MMA warp
         }
         for (int a = 0; a < ACC; ++a) {
@@ -283,10 +300,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_a);
-        if (!C_::ACT) prefetch_tensormap(&tm_b);  // resident activations: no B map
+        if (!C_::ACT && !C_::SACT) prefetch_tensormap(&tm_b);  // activations quantized here: no B map
         if (!p.sf_rowmajor) {
             prefetch_tensormap(&tm_sfa);
-            if (!C_::ACT) prefetch_tensormap(&tm_sfb);
+            if (!C_::ACT && !C_::SACT) prefetch_tensormap(&tm_sfb);
         }
         if (p.use_tma_epi) prefetch_tensormap(&tm_c);
     }
@@ -447,7 +464,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         int stage = 0;
         uint32_t phase = 0;
         // load roles: 0 A, 1 B, 2 A's scales, 3 B's scales (resident activations: A and its scales only)
-        const int li = C_::ACT ? ((lane & 1) ? 2 : 0) : (lane & 3);
+        constexpr bool kNoB = C_::ACT || C_::SACT;  // B is not loaded by TMA
+        const int li = kNoB ? ((lane & 1) ? 2 : 0) : (lane & 3);
         const void* lmap = li == 0 ? (const void*)&tm_a : li == 1 ? (const void*)&tm_b
                                                     : li == 2 ? (const void*)&tm_sfa : (const void*)&tm_sfb;
         const uint32_t lbase = smem_u32(smem) + (li == 0 ? C_::OFF_A : li == 1 ? C_::OFF_B
@@ -485,11 +503,11 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // operand maps are 3-D; boxes past the tensor's end read zeros
                 // and count their full bytes.
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&full[stage], p.tx_a + (C_::ACT ? 0u : p.tx_b) +
+                    mbar_arrive_expect_tx(&full[stage], p.tx_a + (kNoB ? 0u : p.tx_b) +
                                                             (p.sf_rowmajor ? 0u : C_::SF_TX));
                 {
                     const int kbg = kb + p.k_atom0;  // stage of K in the whole tensor
-                    const int nl = (C_::ACT || p.sf_rowmajor) ? 2 : 4;
+                    const int nl = (kNoB || p.sf_rowmajor) ? 2 : 4;
                     const uint32_t dst = lbase + (uint32_t)stage * lstep;
                     const int32_t y = li == 0 ? p0 : li == 1 ? q0 : 4 * C_::GS * kbg;
                     const int32_t z = li < 2 ? SA * kbg : (li == 2 ? w.tp : q0 >> 7);
@@ -695,6 +713,116 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     phase ^= 1;
                 }
             }
+        }
+    } else if (C_::SACT && warp >= C_::ACT_WARP0) {
+        if constexpr (C_::SACT) {
+        // -------------------------------------------- streamed activations
+        // Activation warp aw fills the B slot (codes and scale tile) of every
+        // ACT_WARPS-th stage of the CTA's schedule, starting at stage aw: it
+        // loads the stage's BN rows x SA atoms of bf16 activations (from
+        // L2 after the first CTA's touch), quantizes them with mx_quantize's
+        // rounding into the MMA operand layout (128-byte swizzled rows, the
+        // tensor-core scale tile), waits for the slot to be free, writes it
+        // and arrives on the stage's full barrier beside the TMA bytes.  Lane l
+        // takes 32-element blocks l, l + 32, .. of the stage (row-major over
+        // rows x blocks, so a warp's loads are contiguous); rows past M become
+        // zero codes.  Loads and arithmetic happen before the slot wait, so
+        // they overlap the MMAs still reading it.
+        constexpr int BPA = KIND == KIND_F4 ? 8 : 4;   // 32-element blocks per atom
+        constexpr int BPS = SA * BPA;                  // blocks per stage and row
+        constexpr int PER_LANE = BN * BPS / 32;
+        constexpr int AFMT = KIND == KIND_F4 ? FMT_E2M1 : FMT_E4M3;
+        constexpr int CW = AFMT == FMT_E2M1 ? 4 : 8;   // code words per block
+        const int aw = warp - C_::ACT_WARP0;
+        int n = 0;  // the CTA's stage counter (identical in every role)
+        bool live = true;
+        Work w;
+        for (int it = 0; live && work_at(it, w); ++it) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++n) {
+                if (n % C_::ACT_WARPS != aw) continue;
+                const int stage = n % STAGES;
+                const int64_t k_stage = (int64_t)(kb + p.k_atom0) * BPS * 32;  // first element of the stage
+                uint8_t* bslot = smem + C_::OFF_B + stage * C_::B_BYTES;
+                uint8_t* sfslot = smem + C_::OFF_SFB + stage * C_::SFB_BYTES;
+                // KB blocks' loads are issued before any of them is converted;
+                // the first batch's loads are in flight while the slot is
+                // awaited (it is free once the MMAs of its previous fill have
+                // read it; the first STAGES fills find it free)
+                auto fill = [&](auto words_tag, auto kb_tag) -> bool {
+                    constexpr int WORDS = decltype(words_tag)::value;  // 16 (bf16) or 32 (f32)
+                    constexpr int KB = decltype(kb_tag)::value;
+                    static_assert(PER_LANE % KB == 0, "whole load batches");
+#pragma unroll
+                    for (int b0 = 0; b0 < PER_LANE; b0 += KB) {
+                        uint32_t raw[KB][WORDS];
+#pragma unroll
+                        for (int q = 0; q < KB; ++q) {
+                            const int i = lane + 32 * (b0 + q);
+                            const int r = i / BPS;
+                            const int64_t k = k_stage + (int64_t)(i % BPS) * 32;
+                            if (r < p.Q) {
+                                const uint4* src = reinterpret_cast<const uint4*>(
+                                    static_cast<const uint8_t*>(p.act) + ((int64_t)r * p.act_ld + k) * (WORDS / 8));
+#pragma unroll
+                                for (int t = 0; t < WORDS / 4; ++t) {
+                                    const uint4 v = __ldg(src + t);
+                                    raw[q][4 * t] = v.x;
+                                    raw[q][4 * t + 1] = v.y;
+                                    raw[q][4 * t + 2] = v.z;
+                                    raw[q][4 * t + 3] = v.w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int t = 0; t < WORDS; ++t) raw[q][t] = 0;
+                            }
+                        }
+                        if (b0 == 0) {
+                            int okw = 1;
+                            if (lane == 0 && n >= STAGES)
+                                okw = mbar_wait(&empty[stage], ((uint32_t)(n / STAGES) & 1u) ^ 1u, p.wait_limit_ns,
+                                                err);
+                            if (!__shfl_sync(0xFFFFFFFFu, okw, 0)) return false;
+                        }
+#pragma unroll
+                        for (int q = 0; q < KB; ++q) {
+                            uint32_t u[32];
+#pragma unroll
+                            for (int t = 0; t < 32; ++t)
+                                u[t] = WORDS == 32 ? raw[q][t]
+                                                   : ((t & 1) ? (raw[q][t >> 1] & 0xFFFF0000u) : (raw[q][t >> 1] << 16));
+                            uint32_t out[CW];
+                            const uint32_t sb = quantize_column_block<AFMT>(u, WORDS == 16, out);
+                            const int i = lane + 32 * (b0 + q);
+                            const int r = i / BPS, j = i % BPS;
+                            const int a = j / BPA, jj = j % BPA;  // atom of the stage, block of the atom
+                            uint8_t* rowp = bslot + a * C_::B_ATOM + r * kRowBytes;
+                            if constexpr (AFMT == FMT_E4M3) {  // 32 bytes: 16-byte chunks 2jj, 2jj + 1
+                                *reinterpret_cast<uint4*>(rowp + (((2 * jj) ^ (r & 7)) << 4)) =
+                                    make_uint4(out[0], out[1], out[2], out[3]);
+                                *reinterpret_cast<uint4*>(rowp + (((2 * jj + 1) ^ (r & 7)) << 4)) =
+                                    make_uint4(out[4], out[5], out[6], out[7]);
+                            } else {  // packed E2M1: 16 bytes, chunk jj
+                                *reinterpret_cast<uint4*>(rowp + ((jj ^ (r & 7)) << 4)) =
+                                    make_uint4(out[0], out[1], out[2], out[3]);
+                            }
+                            sfslot[(a * C_::G + jj / 4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (jj & 3)] =
+                                (uint8_t)sb;
+                        }
+                    }
+                    return true;
+                };
+                // (bf16 activations only: the host routes f32 to the resident path)
+                const bool okf = fill(std::integral_constant<int, 16>(), std::integral_constant<int, 4>());
+                if (!okf) {
+                    live = false;
+                    if (lane == 0) *abort_flag = 1;
+                    break;
+                }
+                fence_proxy_async_smem();  // generic writes, read by the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[stage]);
+            }
+        }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -1701,6 +1829,29 @@ cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t st, const
         return cudaErrorInvalidValue;
     }
     const int64_t total = (a.K + sa * k_per_stage - 1) / (sa * k_per_stage);
+    if (sa == 2 && bn == 16 && a.act_dtype == DT_BF16) {
+        // up to 16 rows of bf16, two-atom stages: activations quantized stage
+        // by stage into the ring (any K in one launch).  f32 activations take
+        // the resident path: their exact rounding costs several times the
+        // arithmetic of bf16's, which four warps cannot keep up with per stage.
+        p.k_atom0 = 0;
+        p.k_stages = (int32_t)total;
+        const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
+        p.total_units = tiles * p.k_stages;
+        const int sms = sm_count();
+        int grid;
+        if (tiles >= sms || p.k_stages < 4) {
+            p.mode = 0;
+            grid = (int)(tiles < sms ? tiles : sms);
+        } else {
+            p.mode = 1;
+            grid = (int)(p.total_units < sms ? p.total_units : sms);
+        }
+        CUtensorMap none;
+        std::memset(&none, 0, sizeof(none));
+        if (kind == KIND_F4) return run<KIND_F4, 16, 5, 1, 0, kActStreamed, 2>(ta, none, tsa, none, tc, p, grid, st);
+        return run<KIND_F8F6F4, 16, 5, 1, 0, kActStreamed, 2>(ta, none, tsa, none, tc, p, grid, st);
+    }
 #define MX_ACT2(KIND_, BN_, ST_, AT_) return run_act_chunks<KIND_, BN_, ST_, AT_, 2>(a, ta, tsa, tc, p, total, st)
     if (sa == 2) {
         if (kind == KIND_F4) {
