@@ -672,8 +672,11 @@ def main():
     if not args.no_gemm:
         mma = mma_rates(mx)
         for cfg in (3, 4, 5):
-            gemms.append(bench_gemm(mx, cfg, args.gemm_steps, max(3, args.warmup), world, peaks, 1.0, dev_index, mma))
-    nxt = None if args.no_gemm else bench_next(mx, args.gemm_steps, max(3, args.warmup), world, peaks, dev_index)
+            # kernels of a few microseconds get 13x the steps, so a timed
+            # region is whole graphs of hundreds of launches
+            st = args.gemm_steps * (13 if cfg == 3 else 1)
+            gemms.append(bench_gemm(mx, cfg, st, max(3, args.warmup), world, peaks, 1.0, dev_index, mma))
+    nxt = None if args.no_gemm else bench_next(mx, args.gemm_steps * 13, max(3, args.warmup), world, peaks, dev_index)
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(hl["x_host"])

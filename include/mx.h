@@ -222,7 +222,10 @@ MX_API mx_status_t mx_block_matmul_f32b(const void* a_codes, const uint8_t* a_sc
  * (quantize A once with mx_quantize and call mx_block_matmul: a larger A would
  * be quantized again for every column tile).  Formats: E4M3FN activations
  * with E4M3FN or E2M1 weights, E2M1 activations with E2M1 weights.  `a` must
- * be 32-B aligned; other rules, results and tolerance as mx_block_matmul. */
+ * be 32-B aligned; other rules, results and tolerance as mx_block_matmul.
+ * Speed: bf16 activations with M <= 16 and K a multiple of 256 (E4M3FN
+ * activations) or 512 (E2M1) match mx_quantize + mx_block_matmul in one
+ * launch; f32 activations take about twice as long as those two calls. */
 MX_API mx_status_t mx_block_matmul_act(const void* a, mx_dtype_t a_dtype, mx_format_t a_fmt, const void* b_codes,
                                 const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t b_scale_layout,
                                 int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
