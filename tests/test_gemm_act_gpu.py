@@ -106,3 +106,62 @@ def test_fused_equals_quantize_then_gemm_bitwise(fa, fb, dtype, M, N):
     mx.mx_block_matmul(ac, as_, fa, bc, bs, fb, M, N, K, C2, mx.SCALES_MMA)
     mx.mx_device_status()
     assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+
+
+# ------------------------------------------- bf16 activations streamed by stage
+# Up to 16 bf16 rows with K a whole number of two-atom stages (256 elements for
+# E4M3FN activations, 512 for E2M1): the activations are quantized stage by
+# stage into the kernel's ring.  Everything else takes the resident path above.
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (1, 130, 256, mx.E4M3FN, mx.E4M3FN),       # one stage, one real row
+    (5, 1000, 1024, mx.E4M3FN, mx.E2M1),       # ragged weight tiles, split along K
+    (16, 2052, 768, mx.E4M3FN, mx.E4M3FN),     # three stages
+    (16, 1030, 512, mx.E4M3FN, mx.E2M1),       # N % 4 != 0: per-element epilogue
+    (9, 384, 4096, mx.E2M1, mx.E2M1),          # packed FP4 stages of 512
+    (16, 19500, 256, mx.E4M3FN, mx.E4M3FN),    # more tiles than SMs: whole tiles
+])
+def test_streamed_shapes(M, N, K, fa, fb):
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = torch.from_numpy(randn(rng, (M, K)) * np.float32(2.0) ** rng.integers(-6, 6, (M, 1)).astype(np.float32))
+    fused_vs_oracle(A.to(torch.bfloat16), randn(rng, (N, K), 0.05), fa, fb, randn(rng, (M, N)))
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (16, 1000, 768, mx.E4M3FN, mx.E2M1),       # three stages
+    (3, 384, 512, mx.E4M3FN, mx.E4M3FN),       # two stages
+    (16, 512, 1024, mx.E2M1, mx.E2M1),         # two FP4 stages
+    (16, 19500, 256, mx.E4M3FN, mx.E4M3FN),    # more tiles than SMs
+])
+def test_streamed_equals_quantize_then_gemm_bitwise(M, N, K, fa, fb):
+    # same MMAs, same schedule as mx_quantize + mx_block_matmul: equal bit for
+    # bit on shapes whose tiles each stay on one CTA (fewer than four stages,
+    # or more tiles than SMs); split along K, partial sums meet in C through
+    # reduce-adds in whatever order they land, so only the tolerance holds
+    rng = np.random.default_rng(M + N + K)
+    A = torch.from_numpy(randn(rng, (M, K)) * np.float32(3.0)).to(torch.bfloat16)
+    bc, bs = weights(randn(rng, (N, K)), fb)
+    C0 = randn(rng, (M, N))
+    C1 = torch.from_numpy(C0).cuda()
+    mx.mx_block_matmul_act(A.cuda(), fa, bc, bs, fb, N, C1)
+    ac, as_ = mx.alloc_codes(M, K, fa), mx.alloc_scales(M, K, mx.SCALES_MMA)
+    mx.mx_quantize(A.cuda(), fa, ac, as_, mx.SCALES_MMA)
+    C2 = torch.from_numpy(C0).cuda()
+    mx.mx_block_matmul(ac, as_, fa, bc, bs, fb, M, N, K, C2, mx.SCALES_MMA)
+    mx.mx_device_status()
+    assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+
+
+def test_streamed_special_values():
+    # bf16: zero rows, a NaN and an infinity (their blocks' scales 0xFF poison
+    # their products), subnormals, negative zeros
+    rng = np.random.default_rng(37)
+    M, N, K = 16, 256, 512
+    A = randn(rng, (M, K))
+    A[1] = 0.0
+    A[2, 40] = np.nan
+    A[5, 300] = -np.inf
+    A[3] = np.float32(2.0 ** -130) * np.arange(K, dtype=np.float32)
+    A[4, :32] = -0.0
+    fused_vs_oracle(torch.from_numpy(A).to(torch.bfloat16), randn(rng, (N, K)), mx.E4M3FN, mx.E2M1,
+                    np.zeros((M, N), np.float32))
