@@ -1832,8 +1832,9 @@ cudaError_t launch_block_matmul_act(const GemmActArgs& a, cudaStream_t st, const
     if (sa == 2 && bn == 16 && a.act_dtype == DT_BF16) {
         // up to 16 rows of bf16, two-atom stages: activations quantized stage
         // by stage into the ring (any K in one launch).  f32 activations take
-        // the resident path: their exact rounding costs several times the
-        // arithmetic of bf16's, which four warps cannot keep up with per stage.
+        // the resident path: a stage's f32 blocks are twice the registers of
+        // bf16's, so four warps would load them in two batches per stage
+        // (measured slower than the resident path on the decode shape).
         p.k_atom0 = 0;
         p.k_stages = (int32_t)total;
         const int64_t tiles = (int64_t)p.tiles_p * p.tiles_q;
