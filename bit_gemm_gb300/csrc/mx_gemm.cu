@@ -22,6 +22,8 @@
 //   gate warp   waits on each stage's barrier and passes it to the MMA warp(s)
 //               through a named barrier, so the issuing thread never touches
 //               shared memory between MMAs.
+//   act warps   (decode shapes with bf16 activations quantized in the kernel)
+//               quantize each stage's activations into the ring's B slot.
 //   epilogue    4 or 8 warps: TMEM -> registers -> swizzled shared staging ->
 //               TMA reduce-add into C (C += acc, performed at L2), so C is read
 //               and written in place with no extra pass.
@@ -185,6 +187,7 @@ struct Cfg {
     // n - ACT_WARPS - STAGES was consumed, and fill n needs n - 2 STAGES, so
     // ACT_WARPS may not exceed STAGES.
     static_assert(ACT_WARPS <= STAGES, "activation warps at most one ring phase ahead");
+    static_assert(32 * (PRO_WARPS + 1) <= THREADS, "warps 1..PRO_WARPS exist");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(SWAP || BN % 128 == 0, "B tiles start on 128-row boundaries");
     static_assert(SMEM <= 232448, "shared memory per CTA");
