@@ -1417,10 +1417,6 @@ bool make_operand_map3n(CUtensorMap* m, const void* codes, int64_t rows, int64_t
     return r == CUDA_SUCCESS;
 }
 
-bool make_operand_map3(CUtensorMap* m, const void* codes, int64_t rows, int64_t K, int fmt_kind, int box_rows) {
-    return make_operand_map3n(m, codes, rows, K, fmt_kind, box_rows, 1);
-}
-
 // Tensor map over C (rows x cols f32, row-major) for the reduce-add epilogue.
 bool make_c_map(CUtensorMap* m, float* C, int64_t rows, int64_t cols, int box_cols, int box_rows, int swizzle) {
     EncodeTiledFn enc = encode_fn();
