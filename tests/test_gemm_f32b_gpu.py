@@ -22,11 +22,14 @@ def check(got, ref, sabs, c0, where):
     got = np.asarray(got, np.float64)
     nan_ref = np.isnan(ref)
     assert np.isnan(got[nan_ref]).all(), f"{where}: NaN expected"
-    ok = ~nan_ref
+    inf_ref = np.isinf(ref)
+    assert (got[inf_ref] == ref[inf_ref]).all(), f"{where}: infinity expected"
+    ok = ~(nan_ref | inf_ref)
     err = np.abs(got[ok] - ref[ok])
     tol = REL * sabs[ok] + np.abs(ref[ok]) * 2.0 ** -23
     zero = sabs[ok] == 0
-    bad = (err > tol) | (zero & (got[ok] != np.asarray(c0, np.float64)[ok]))
+    # a NaN or an infinity where the reference is finite fails too
+    bad = ~(err <= tol) | (zero & (got[ok] != np.asarray(c0, np.float64)[ok]))
     assert not bad.any(), f"{where}: {bad.sum()} of {bad.size} entries outside tolerance"
 
 
