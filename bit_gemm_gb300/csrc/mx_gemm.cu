@@ -41,7 +41,6 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
-#include <type_traits>
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
@@ -751,9 +750,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // the first batch's loads are in flight while the slot is
                 // awaited (it is free once the MMAs of its previous fill have
                 // read it; the first STAGES fills find it free)
-                auto fill = [&](auto words_tag, auto kb_tag) -> bool {
-                    constexpr int WORDS = decltype(words_tag)::value;  // 16 (bf16) or 32 (f32)
-                    constexpr int KB = decltype(kb_tag)::value;
+                // (bf16 activations only: the host routes f32 to the resident path)
+                auto fill = [&]() -> bool {
+                    constexpr int WORDS = 16;  // one block of 32 bf16, two per word (lower element low)
+                    constexpr int KB = 4;      // blocks per load batch
                     static_assert(PER_LANE % KB == 0, "whole load batches");
 #pragma unroll
                     for (int b0 = 0; b0 < PER_LANE; b0 += KB) {
@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                             const int64_t k = k_stage + (int64_t)(i % BPS) * 32;
                             if (r < p.Q) {
                                 const uint4* src = reinterpret_cast<const uint4*>(
-                                    static_cast<const uint8_t*>(p.act) + ((int64_t)r * p.act_ld + k) * (WORDS / 8));
+                                    static_cast<const __nv_bfloat16*>(p.act) + (int64_t)r * p.act_ld + k);
 #pragma unroll
                                 for (int t = 0; t < WORDS / 4; ++t) {
                                     const uint4 v = __ldg(src + t);
@@ -788,13 +788,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                         }
 #pragma unroll
                         for (int q = 0; q < KB; ++q) {
-                            uint32_t u[32];
-#pragma unroll
-                            for (int t = 0; t < 32; ++t)
-                                u[t] = WORDS == 32 ? raw[q][t]
-                                                   : ((t & 1) ? (raw[q][t >> 1] & 0xFFFF0000u) : (raw[q][t >> 1] << 16));
                             uint32_t out[CW];
-                            const uint32_t sb = quantize_column_block<AFMT>(u, WORDS == 16, out);
+                            const uint32_t sb = quantize_block_bf16<AFMT>(raw[q], out);  // word t: elements 2t, 2t + 1
                             const int i = lane + 32 * (b0 + q);
                             const int r = i / BPS, j = i % BPS;
                             const int a = j / BPA, jj = j % BPA;  // atom of the stage, block of the atom
@@ -814,8 +809,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     }
                     return true;
                 };
-                // (bf16 activations only: the host routes f32 to the resident path)
-                const bool okf = fill(std::integral_constant<int, 16>(), std::integral_constant<int, 4>());
+                const bool okf = fill();
                 if (!okf) {
                     live = false;
                     if (lane == 0) *abort_flag = 1;
