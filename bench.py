@@ -162,45 +162,68 @@ def sets_for(bytes_per_step: int) -> int:
     return max(2, math.ceil(3 * l2_bytes() / bytes_per_step))
 
 
-def timed_graph_steps(step_fn, nsets: int, steps: int, warmup: int, world: int):
-    """Run `warmup` eager steps, then exactly `steps` steps from CUDA graphs,
-    timed with events on the capturing stream.  Returns (seconds, launches per step).
-    step_fn(i) issues the work of step i on the current stream."""
+def timed_graph_steps(step_fn, nsets: int, steps: int, warmup: int, world: int, dist_replays: int = 20):
+    """Run `warmup` eager steps, then exactly `steps` steps replayed from CUDA
+    graphs on one stream, between CUDA events on that stream: a graph of up
+    to 256 steps (a whole number of rotations) replayed as often as fits, and
+    a shorter graph for the remainder.  Afterwards, outside that timed
+    region, the main graph is replayed `dist_replays` more times, each between
+    its own events, for the spread of the per-step time.  Returns (seconds for
+    the `steps` steps, seconds per step of each extra replay).  step_fn(i)
+    issues step i."""
     for i in range(warmup):
         step_fn(i % nsets)
     torch.cuda.synchronize()
-    per_graph = max(nsets, min(steps, 256) // nsets * nsets)
+    n = min(steps, max(nsets, min(steps, 256) // nsets * nsets))
+    reps, rem = divmod(steps, n)
     stream = torch.cuda.Stream()
-    graphs = []
-    counts = []
-    remaining = steps
     with torch.cuda.stream(stream):
-        while remaining > 0 and len(graphs) < 2:
-            n = per_graph if remaining >= per_graph else remaining
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step_fn(i % nsets)
+        g_rem = None
+        if rem:
+            g_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_rem, stream=stream):
+                for i in range(rem):
                     step_fn(i % nsets)
-            reps = remaining // n if len(graphs) == 0 else 1
-            graphs.append(g)
-            counts.append(reps)
-            remaining -= reps * n
-        assert remaining == 0
         torch.cuda.synchronize()
-        graphs[0].replay()  # upload / first-replay cost kept out of the timed region
+        g.replay()  # upload / first-replay cost kept out of the timed region
+        if g_rem is not None:
+            g_rem.replay()
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for g, reps in zip(graphs, counts):
-            for _ in range(reps):
-                g.replay()
+        for _ in range(reps):
+            g.replay()
+        if g_rem is not None:
+            g_rem.replay()
         end.record(stream)
         torch.cuda.synchronize()
+        barrier(world)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(dist_replays + 1)]
+        evs[0].record(stream)
+        for r in range(dist_replays):
+            g.replay()
+            evs[r + 1].record(stream)
+        torch.cuda.synchronize()
     barrier(world)
-    return start.elapsed_time(end) / 1e3
+    per_step = [evs[r].elapsed_time(evs[r + 1]) / 1e3 / n for r in range(dist_replays)]
+    return start.elapsed_time(end) / 1e3, per_step
+
+
+def dist_us(per_step):
+    """Median and 10th / 90th percentiles of per-step times, in microseconds
+    (one value per graph replay: its time over its steps)."""
+    if not per_step:
+        return None
+    v = sorted(x * 1e6 for x in per_step)
+    q = lambda f: v[min(len(v) - 1, max(0, int(round(f * (len(v) - 1)))))]
+    return {"median_us": statistics.median(v), "p10_us": q(0.1), "p90_us": q(0.9), "replays": len(v)}
 
 
 # ------------------------------------------------------------- workloads
@@ -214,11 +237,23 @@ def headline_bytes(rows, cols):
     return q, d
 
 
+def timed(step_fn, nsets, steps, warmup, world):
+    """timed_graph_steps with the maximum over ranks of the total; returns (seconds, distribution)."""
+    sec, per = timed_graph_steps(step_fn, nsets, steps, warmup, world)
+    return max_over_ranks(sec, world), dist_us(per)
+
+
 def bench_headline(mx, steps, warmup, world, peaks, device_index):
+    """Workload 2: step i quantizes rotation set i and dequantizes the set
+    written half a rotation earlier (at least 1.5x L2 of traffic ago), so the
+    codes and scales it reads come from HBM like every other counted byte:
+    the step's bytes per second is an HBM rate.  Each kernel is also timed on
+    its own over the same rotation (the roofline's per-kernel numbers)."""
     w = workloads.make(2)
     rows, cols = w["rows"], w["cols"]
     qb, db = headline_bytes(rows, cols)
     nsets = sets_for(qb + db)
+    half = nsets // 2
     x0 = w["x"].cuda()
     sets = []
     for i in range(nsets):
@@ -229,7 +264,8 @@ def bench_headline(mx, steps, warmup, world, peaks, device_index):
     def step(i):
         s = sets[i]
         mx.mx_quantize(s["x"], mx.E4M3FN, s["codes"], s["scales"])
-        mx.mx_dequantize(s["codes"], s["scales"], rows, cols, mx.E4M3FN, s["y"])
+        d = sets[(i + half) % nsets]
+        mx.mx_dequantize(d["codes"], d["scales"], rows, cols, mx.E4M3FN, d["y"])
 
     def deq_only(i):
         s = sets[i]
@@ -239,30 +275,34 @@ def bench_headline(mx, steps, warmup, world, peaks, device_index):
         s = sets[i]
         mx.mx_quantize(s["x"], mx.E4M3FN, s["codes"], s["scales"])
 
-    # correctness of what is timed: the 64 NaN-scale blocks poison their blocks
-    step(0)
+    # every set holds codes before a step dequantizes it; correctness of what
+    # is timed: the 64 NaN-scale blocks poison their blocks
+    for i in range(nsets):
+        q_only(i)
     s0 = sets[0]
     s0["scales"][nan_blocks] = 0xFF
-    mx.mx_dequantize(s0["codes"], s0["scales"], rows, cols, mx.E4M3FN, s0["y"])
+    deq_only(0)
     mx.mx_device_status()
     assert int(torch.isnan(s0["y"].view(-1, 32)).all(dim=1).sum()) >= 64
+    q_only(0)
 
     with ClockSampler(device_index) as clk:
-        sec = timed_graph_steps(step, nsets, steps, warmup, world)
-    sec = max_over_ranks(sec, world)
+        sec, dist = timed(step, nsets, steps, warmup, world)
     value = job_throughput((qb + db) * steps, world, sec) / 1e9
     # per-kernel timing for the roofline (same stream, same rotation)
     k_steps = max(steps, 200)
-    sec_d = max_over_ranks(timed_graph_steps(deq_only, nsets, k_steps, 3, world), world)
-    sec_q = max_over_ranks(timed_graph_steps(q_only, nsets, k_steps, 3, world), world)
+    sec_d, dist_d = timed(deq_only, nsets, k_steps, 3, world)
+    sec_q, dist_q = timed(q_only, nsets, k_steps, 3, world)
     deq_gbs = db * k_steps / sec_d / 1e9
     q_gbs = qb * k_steps / sec_q / 1e9
     mx.mx_device_status()
     return {
-        "value": value, "ms_per_step": sec / steps * 1e3, "clocks": clk.summary(), "nsets": nsets,
+        "value": value, "ms_per_step": sec / steps * 1e3, "dist": dist, "clocks": clk.summary(), "nsets": nsets,
         "launches": 2 * steps,
-        "quantize": {"gbs": q_gbs, "us": sec_q / k_steps * 1e6, "bytes": qb, "frac": q_gbs / peaks["hbm_gbs"]},
-        "dequantize": {"gbs": deq_gbs, "us": sec_d / k_steps * 1e6, "bytes": db, "frac": deq_gbs / peaks["hbm_gbs"]},
+        "quantize": {"gbs": q_gbs, "us": sec_q / k_steps * 1e6, "bytes": qb, "frac": q_gbs / peaks["hbm_gbs"],
+                     "dist": dist_q},
+        "dequantize": {"gbs": deq_gbs, "us": sec_d / k_steps * 1e6, "bytes": db, "frac": deq_gbs / peaks["hbm_gbs"],
+                       "dist": dist_d},
         "dominant": "dequantize" if sec_d >= sec_q else "quantize",
         "x_host": w["x"], "rows": rows, "cols": cols, "bytes": qb + db,
     }
@@ -364,9 +404,22 @@ def mma_rates(mx):
     return {"fp8": mx.mx_measure_mma_rate(mx.E4M3FN, 20000), "fp4": mx.mx_measure_mma_rate(mx.E2M1, 20000)}
 
 
-def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma=None):
+def tensor_peak(peaks, mma, kind):
+    """The GEMM roofline's denominator: the larger of the recipe figure
+    (measured bf16 burst x the nominal dense ratio of the format) and this
+    GPU's measured block-scaled MMA rate."""
+    recipe = peaks["bf16_tflops"] * NOMINAL_RATIO[kind]
+    measured = mma[kind] if mma else None
+    if measured is not None and measured > recipe:
+        return measured, "measured block-scaled MMA rate (mx_measure_mma_rate)"
+    return recipe, f"measured bf16 burst x {NOMINAL_RATIO[kind]:g} (nominal dense ratio)"
+
+
+def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma=None, oracle_rows=0):
     """block_matmul workloads.  Weights are quantized before timing; the step
-    includes the activation quantize where the workload quantizes on the fly."""
+    includes the activation quantize where the workload quantizes on the fly,
+    and that quantize is also timed on its own.  oracle_rows > 0: the CPU
+    oracle's block_matmul and activation quantize are timed too (rank 0)."""
     w = workloads.make(cfg, scale=scale)
     M, N, K = w["M"], w["N"], w["K"]
     if cfg == 3:
@@ -385,7 +438,8 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
     a_bytes_in = A.numel() * A.element_size()
     ca_b, sa_b = mx.mx_codes_bytes(fa, M, K), mx.mx_scales_bytes(L, M, K)
     gemm_bytes = ca_b + sa_b + mx.mx_codes_bytes(fb, N, K) + mx.mx_scales_bytes(L, N, K) + 8 * M * N
-    step_bytes = gemm_bytes + (a_bytes_in + ca_b + sa_b if quant_a else 0)
+    qa_bytes = a_bytes_in + ca_b + sa_b
+    step_bytes = gemm_bytes + (qa_bytes if quant_a else 0)
     nsets = sets_for(step_bytes) if step_bytes < 3 * l2_bytes() else 1
     # rotate only what fits; the weight (B) is shared, A and C rotate
     sets = []
@@ -415,6 +469,10 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
         s = sets[i]
         mx.mx_block_matmul(s["ac"], s["as"], fa, s["bc"], s["bs"], fb, M, N, K, s["C"], L)
 
+    def q_only(i):
+        s = sets[i]
+        mx.mx_quantize(s["A"], fa, s["ac"], s["as"], L)
+
     def fused(i):
         # activations quantized inside the GEMM (one launch; M <= 64 only)
         s = sets[i]
@@ -422,41 +480,52 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
 
     step(0)
     mx.mx_device_status()
-    sec_f = None
+    sec_f = dist_f = sec_q = dist_q = None
     with ClockSampler(dev_index) as clk:
-        sec = max_over_ranks(timed_graph_steps(step, nsets, steps, warmup, world), world)
-        sec_g = max_over_ranks(timed_graph_steps(gemm_only, nsets, steps, 3, world), world)
+        sec, dist = timed(step, nsets, steps, warmup, world)
+        sec_g, dist_g = timed(gemm_only, nsets, steps, 3, world)
+        if quant_a:
+            sec_q, dist_q = timed(q_only, nsets, steps, 3, world)
         if quant_a and M <= 64:
             fused(0)
             mx.mx_device_status()
-            sec_f = max_over_ranks(timed_graph_steps(fused, nsets, steps, 3, world), world)
+            sec_f, dist_f = timed(fused, nsets, steps, 3, world)
     mx.mx_device_status()
     flops = 2.0 * M * N * K
     tf_step = job_throughput(flops * steps, world, sec) / 1e12
     tf_gemm = flops * steps / sec_g / 1e12
-    peak_tf = peaks["bf16_tflops"] * NOMINAL_RATIO[kind]
+    peak_tf, peak_src = tensor_peak(peaks, mma, kind)
     gbs_gemm = gemm_bytes * steps / sec_g / 1e9
     out = {"workload": workloads.NAMES[cfg], "M": M, "N": N, "K": K, "formats": {
         3: "E4M3 x E2M1", 4: "E4M3 x E4M3", 5: "E2M1 x E2M1"}[cfg],
         "step": "quantize A + block_matmul" if quant_a else "block_matmul",
-        "tflops_step": tf_step, "us_per_step": sec / steps * 1e6,
-        "tflops_gemm": tf_gemm, "us_gemm": sec_g / steps * 1e6,
-        "tensor_peak_tflops": peak_tf, "tensor_frac": tf_gemm / peak_tf,
+        "tflops_step": tf_step, "us_per_step": sec / steps * 1e6, "step_dist": dist,
+        "tflops_gemm": tf_gemm, "us_gemm": sec_g / steps * 1e6, "gemm_dist": dist_g,
+        "tensor_peak_tflops": peak_tf, "tensor_peak_source": peak_src, "tensor_frac": tf_gemm / peak_tf,
+        "tensor_frac_of_recipe": tf_gemm / (peaks["bf16_tflops"] * NOMINAL_RATIO[kind]),
         "gemm_gbs": gbs_gemm, "hbm_frac": gbs_gemm / peaks["hbm_gbs"], "gemm_bytes": gemm_bytes,
         "launches_per_step": 2 if quant_a else 1, "nsets": nsets, "clocks": clk.summary()}
     if mma is not None:
         out["mma_measured_tflops"] = mma[kind]
         out["tensor_frac_of_mma_measured"] = tf_gemm / mma[kind]
+    if sec_q is not None:
+        g = qa_bytes * steps / sec_q / 1e9
+        out["act_quantize"] = {"what": f"{'bf16' if A.dtype == torch.bfloat16 else 'f32'} {M}x{K} -> "
+                                       f"{'MXFP8' if fa == mx.E4M3FN else 'MXFP4'} (tensor-core scale layout)",
+                               "us": sec_q / steps * 1e6, "dist": dist_q, "gbs": g,
+                               "hbm_frac": g / peaks["hbm_gbs"], "bytes": qa_bytes}
     if sec_f is not None:
         # one launch: activations in (f32/bf16), weight codes and scales, C read and written
         fused_bytes = a_bytes_in + mx.mx_codes_bytes(fb, N, K) + mx.mx_scales_bytes(L, N, K) + 8 * M * N
         out["fused"] = {"step": "block_matmul_act (activations quantized in the GEMM)",
-                        "us_per_step": sec_f / steps * 1e6, "tflops": flops * steps / sec_f / 1e12,
+                        "us_per_step": sec_f / steps * 1e6, "dist": dist_f, "tflops": flops * steps / sec_f / 1e12,
                         "gbs": fused_bytes * steps / sec_f / 1e9,
                         "hbm_frac": fused_bytes * steps / sec_f / 1e9 / peaks["hbm_gbs"], "bytes": fused_bytes,
                         "launches_per_step": 1}
     del sets, A, C0, bc, bs
     torch.cuda.empty_cache()
+    if oracle_rows > 0:
+        out["oracle"] = oracle_gemm_baseline(w, cfg, a_key, b_key, quant_a, oracle_rows)
     return out
 
 
@@ -485,7 +554,7 @@ def bench_next(mx, steps, warmup, world, peaks, dev_index):
     f32b(0)
     mx.mx_device_status()
     with ClockSampler(dev_index) as clk:
-        sec = max_over_ranks(timed_graph_steps(f32b, 1, steps, warmup, world), world)
+        sec, dist = timed(f32b, 1, steps, warmup, world)
     mx.mx_device_status()
     ck = clk.summary()
     flops = 2.0 * M * N * K
@@ -495,7 +564,8 @@ def bench_next(mx, steps, warmup, world, peaks, dev_index):
     alu_peak = sms * FFMA_PER_SM_CLK * 2 * mhz * 1e6 / 1e12
     out["block_matmul_f32b"] = {
         "workload": workloads.NAMES[6], "M": M, "N": N, "K": K, "formats": "E4M3 x f32",
-        "us_per_step": sec / steps * 1e6, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"], "bytes": f_bytes,
+        "us_per_step": sec / steps * 1e6, "dist": dist, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+        "bytes": f_bytes,
         "tflops": flops * steps / sec / 1e12, "ffma_peak_tflops": alu_peak,
         "alu_frac": flops * steps / sec / 1e12 / alu_peak, "launches_per_step": 1, "clocks": ck}
     del B, C, ac, as_, w
@@ -529,19 +599,45 @@ def bench_next(mx, steps, warmup, world, peaks, dev_index):
         q_axis0(i)
     mx.mx_device_status()
     k = max(steps, 200)
-    sec_q = max_over_ranks(timed_graph_steps(q_axis0, nsets, k, 3, world), world)
-    sec_d = max_over_ranks(timed_graph_steps(deq_bf16, nsets, k, 3, world), world)
-    sec_f = max_over_ranks(timed_graph_steps(fold, nsets, k, 3, world), world)
+    sec_q, dist_q = timed(q_axis0, nsets, k, 3, world)
+    sec_d, dist_d = timed(deq_bf16, nsets, k, 3, world)
+    sec_f, dist_f = timed(fold, nsets, k, 3, world)
     mx.mx_device_status()
-    for name, b, sec_k, what in (("quantize_axis0", qb, sec_q, "bf16 4096x4096 -> MXFP8, blocks down the columns"),
-                                 ("dequantize_bf16", db, sec_d, "MXFP8 4096x4096 -> bf16"),
-                                 ("fold_scale", fb, sec_f, "scale bytes of a 4096x4096 MX tensor, times 2")):
+    for name, b, sec_k, dk, what in (
+            ("quantize_axis0", qb, sec_q, dist_q, "bf16 4096x4096 -> MXFP8, blocks down the columns"),
+            ("dequantize_bf16", db, sec_d, dist_d, "MXFP8 4096x4096 -> bf16"),
+            ("fold_scale", fb, sec_f, dist_f, "scale bytes of a 4096x4096 MX tensor, times 2")):
         g = b * k / sec_k / 1e9
-        out[name] = {"what": what, "us": sec_k / k * 1e6, "gbs": g, "hbm_frac": g / peaks["hbm_gbs"], "bytes": b,
-                     "nsets": nsets}
+        out[name] = {"what": what, "us": sec_k / k * 1e6, "dist": dk, "gbs": g, "hbm_frac": g / peaks["hbm_gbs"],
+                     "bytes": b, "nsets": nsets}
     del sets, x0
     torch.cuda.empty_cache()
     return out
+
+
+TRAFFIC_ROWS = TRAFFIC_COLS = 16384
+
+
+def traffic_case(mx, launches):
+    """The headline kernels on a bf16 16384 x 16384 tensor (seeded N(0,1)):
+    the dequantized f32 output (1 GiB) is eight times L2, so the DRAM bytes an
+    ncu capture counts for one launch are its steady-state traffic (a launch
+    of the 4096 x 4096 workload ends with most of its output still in L2).
+    Runs quantize once, then `launches` dequantize and quantize launches in
+    turn; the capture picks one of each."""
+    torch.manual_seed(0)
+    rows, cols = TRAFFIC_ROWS, TRAFFIC_COLS
+    x = torch.randn(rows, cols, device="cuda").to(torch.bfloat16)
+    codes, scales = mx.alloc_codes(rows, cols, mx.E4M3FN), mx.alloc_scales(rows, cols)
+    y = torch.empty(rows, cols, device="cuda")
+    for _ in range(max(1, launches)):
+        mx.mx_quantize(x, mx.E4M3FN, codes, scales)
+        mx.mx_dequantize(codes, scales, rows, cols, mx.E4M3FN, y)
+    mx.mx_device_status()
+    torch.cuda.synchronize()
+    q, d = headline_bytes(rows, cols)
+    return {"rows": rows, "cols": cols, "launches": launches, "quantize_algorithmic_bytes": q,
+            "dequantize_algorithmic_bytes": d}
 
 
 def measured_traffic(key: str):
@@ -576,19 +672,106 @@ def oracle_step_rate(rows_sample: int, x_full: torch.Tensor, reps: int = 1):
     return dt, (qb + db) * reps
 
 
-def cpu_baseline(x_full: torch.Tensor, target_s: float = 10.0):
-    """The oracle, as it stands, on the host cores: quantize + dequantize of a
-    sample of the headline workload, repeated until about target_s seconds."""
-    import oracle
-    threads = oracle.num_threads()
+class oracle_threads:
+    """Run the oracle with n OpenMP threads inside the block."""
+
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        import oracle
+        self.saved = oracle.num_threads()
+        oracle.set_threads(self.n)
+        return self
+
+    def __exit__(self, *exc):
+        import oracle
+        oracle.set_threads(self.saved)
+        return False
+
+
+def headline_oracle_rate(x_full: torch.Tensor, target_s: float):
+    """Oracle quantize + dequantize of the headline workload: rows sampled and
+    passes repeated until about target_s seconds; returns (GB/s, sample text)."""
     dt, _ = oracle_step_rate(8, x_full)
     per_row = max(dt / 8, 1e-6)
     rows = int(min(x_full.shape[0], max(8, target_s / per_row)))
     reps = max(1, min(50, int(round(target_s / (per_row * rows)))))
     dt, nbytes = oracle_step_rate(rows, x_full, reps)
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows} of 4096 rows of the bf16 4096x4096 workload (quantize + dequantize), "
-                      f"{reps} passes, {dt:.1f} s"}
+    return nbytes / dt / 1e9, f"{rows} of 4096 rows of the bf16 4096x4096 workload (quantize + dequantize), " \
+                              f"{reps} passes, {dt:.1f} s"
+
+
+def cpu_baseline(x_full: torch.Tensor, target_s: float = 8.0):
+    """The oracle, as it stands, on the host cores: quantize + dequantize of a
+    sample of the headline workload, on every core and on one core."""
+    import oracle
+    threads = oracle.num_threads()
+    value, sample = headline_oracle_rate(x_full, target_s)
+    with oracle_threads(1):
+        v1, s1 = headline_oracle_rate(x_full, target_s / 3)
+    # workload 1 in full: quantize A and Bt (f32 128 x 256) to MXFP4, dequantize both, the product
+    w1 = workloads.make(1)
+    t0 = time.perf_counter()
+    (ac, as_), (bc, bs) = oracle.quantize(w1["A"], oracle.E2M1), oracle.quantize(w1["Bt"], oracle.E2M1)
+    t_q = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.dequantize(ac, as_, w1["K"], oracle.E2M1)
+    oracle.dequantize(bc, bs, w1["K"], oracle.E2M1)
+    t_d = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.block_matmul(ac, as_, oracle.E2M1, bc, bs, oracle.E2M1, w1["M"], w1["N"], w1["K"], w1["C0"])
+    t_g = time.perf_counter() - t0
+    return {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "one_core": {"value": v1, "unit": "GB/s", "cores": 1, "sample": s1},
+            "workload1_full_us": {"quantize_A_and_Bt": t_q * 1e6, "dequantize_both": t_d * 1e6,
+                                  "block_matmul": t_g * 1e6}}
+
+
+def oracle_gemm_baseline(w, cfg, a_key, b_key, quant_a, rows_sample):
+    """The oracle's block_matmul (binary64, every element decoded in every
+    product) and, where the workload quantizes its activations, the oracle's
+    quantize of them, on every host core and on one core.  Operands are
+    quantized by the oracle from the workload's host tensors (untimed).  The
+    product runs on min(M, rows_sample) rows of A (every column of B) and is
+    extrapolated linearly in M; one core runs one row."""
+    import oracle
+    fmt = {3: (oracle.E4M3, oracle.E2M1), 4: (oracle.E4M3, oracle.E4M3), 5: (oracle.E2M1, oracle.E2M1)}[cfg]
+    M, N, K = w["M"], w["N"], w["K"]
+    a = w[a_key]
+    a = a.float().numpy() if isinstance(a, torch.Tensor) else np.asarray(a, np.float32)
+    b = w[b_key]
+    b = b.float().numpy() if isinstance(b, torch.Tensor) else np.asarray(b, np.float32)
+    out = {"cores": oracle.num_threads()}
+    if quant_a:
+        in_bytes = M * K * (2 if isinstance(w[a_key], torch.Tensor) and w[a_key].dtype == torch.bfloat16 else 4)
+        nbytes = in_bytes + M * (K // 2 if fmt[0] == oracle.E2M1 else K) + M * (K // 32)
+        t0 = time.perf_counter()
+        oracle.quantize(a, fmt[0])
+        dt = time.perf_counter() - t0
+        out["act_quantize"] = {"s": dt, "gbs": nbytes / dt / 1e9, "rows": M, "sample": "full activation tensor"}
+    bc, bs = oracle.quantize(b, fmt[1])
+    r = min(M, rows_sample)
+    ac, as_ = oracle.quantize(a[:r], fmt[0])
+    c0 = np.ascontiguousarray(w["C0"][:r], np.float32)
+    t0 = time.perf_counter()
+    oracle.block_matmul(ac, as_, fmt[0], bc, bs, fmt[1], r, N, K, c0)
+    dt = time.perf_counter() - t0
+    full_s = dt * M / r
+    out["block_matmul"] = {"s_sample": dt, "rows": r, "s_full_size": full_s,
+                           "tflops": 2.0 * M * N * K / full_s / 1e12,
+                           "sample": "full size" if r == M else f"first {r} of {M} rows, extrapolated linearly in M"}
+    n1 = min(N, 4096)
+    with oracle_threads(1):
+        t0 = time.perf_counter()
+        oracle.block_matmul(ac[:1], as_[:1], fmt[0], bc[:n1], bs[:n1], fmt[1], 1, n1, K,
+                            np.ascontiguousarray(c0[:1, :n1]))
+        d1 = time.perf_counter() - t0
+    out["block_matmul_one_core"] = {"s_sample": d1, "s_full_size": d1 * M * N / n1,
+                                    "tflops": 2.0 * n1 * K / d1 / 1e12,
+                                    "sample": f"1 of {M} rows x {n1} of {N} columns on one core, "
+                                              f"extrapolated linearly in M and N"}
+    return out
 
 
 # ------------------------------------------------------------------- main
@@ -625,6 +808,25 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def summarize(line):
+    """The line's main figures in a few keys (GEMM times in us, fractions of
+    their denominators)."""
+    r3 = lambda v: None if v is None else round(v, 3)
+    out = {"step_hbm_frac": r3(line["hbm_frac"]),
+           "quantize_frac": r3(line["kernels"]["quantize"]["frac"]),
+           "dequantize_frac": r3(line["kernels"]["dequantize"]["frac"])}
+    for g in line["block_matmul"] or []:
+        key = g["workload"].split("_")[0]
+        out[key] = {"gemm_us": round(g["us_gemm"], 1), "tensor_frac": r3(g["tensor_frac"]),
+                    "hbm_frac": r3(g["hbm_frac"]), "step_us": round(g["us_per_step"], 1)}
+        if "act_quantize" in g:
+            out[key]["act_q_us"] = round(g["act_quantize"]["us"], 1)
+            out[key]["act_q_hbm_frac"] = r3(g["act_quantize"]["hbm_frac"])
+        if "fused" in g:
+            out[key]["fused_us"] = round(g["fused"]["us_per_step"], 1)
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -634,10 +836,12 @@ def main():
     ap.add_argument("--gemm-steps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--only", choices=["headline", "decode", "square", "prefill", "next"], default=None,
+    ap.add_argument("--only", choices=["headline", "decode", "square", "prefill", "next", "traffic"], default=None,
                     help="run one workload only, print its numbers and exit (profiling runs)")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="row-count scale of the GEMM workloads with --only (1 = full size)")
+    ap.add_argument("--oracle-rows", type=int, default=16,
+                    help="rows of A in the CPU oracle's timed block_matmul sample (workloads 4 and 5)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -659,6 +863,8 @@ def main():
             out = {k: v for k, v in hl.items() if k not in ("x_host",)}
         elif args.only == "next":
             out = bench_next(mx, args.steps, args.warmup, world, peaks, dev_index)
+        elif args.only == "traffic":
+            out = traffic_case(mx, args.steps)
         else:
             cfg = {"decode": 3, "square": 4, "prefill": 5}[args.only]
             out = bench_gemm(mx, cfg, args.steps, args.warmup, world, peaks, args.scale, dev_index, mma_rates(mx))
@@ -669,17 +875,20 @@ def main():
     e2e = bench_e2e(mx, hl, args.steps, world)
     gemms = []
     mma = None
+    cpu_here = rank == 0 and world == 1 and not args.no_cpu
     if not args.no_gemm:
         mma = mma_rates(mx)
         for cfg in (3, 4, 5):
             # kernels of a few microseconds get 13x the steps, so a timed
             # region is whole graphs of hundreds of launches
             st = args.gemm_steps * (13 if cfg == 3 else 1)
-            gemms.append(bench_gemm(mx, cfg, st, max(3, args.warmup), world, peaks, 1.0, dev_index, mma))
+            gemms.append(bench_gemm(mx, cfg, st, max(3, args.warmup), world, peaks, 1.0, dev_index, mma,
+                                    args.oracle_rows if cpu_here else 0))
     nxt = None if args.no_gemm else bench_next(mx, args.gemm_steps * 13, max(3, args.warmup), world, peaks, dev_index)
     cpu = None
-    if rank == 0 and not args.no_cpu:
+    if cpu_here:
         cpu = cpu_baseline(hl["x_host"])
+        cpu["block_matmul"] = {g["workload"]: g.get("oracle") for g in gemms}
 
     dom = hl[hl["dominant"]]
     traffic = measured_traffic(f"{hl['dominant']}_mxfp8_4096")
@@ -689,9 +898,12 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": HEADLINE, "rows": hl["rows"], "cols": hl["cols"],
                    "bytes_per_step": hl["bytes"], "parallelism": f"replicas x{world}",
-                   "l2": f"rotating {hl['nsets']} buffer sets (> 3x L2) between steps",
-                   "timing": "CUDA graphs of the K steps, events on the launch stream"},
+                   "l2": f"rotating {hl['nsets']} buffer sets (> 3x L2) between steps; each step dequantizes "
+                         f"the set quantized half a rotation earlier, so every counted byte crosses HBM",
+                   "timing": "CUDA graphs of whole rotations, events on the launch stream; step_dist from 20 "
+                             "further replays of the same graph"},
         "hbm_frac": hl["value"] / world / peaks["hbm_gbs"],
+        "step_dist": hl["dist"],
         "roofline": {"bound": "hbm", "kernel": hl["dominant"], "achieved": dom["gbs"], "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": dom["frac"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"],
@@ -702,13 +914,14 @@ def main():
             "recipe_fp8": peaks["bf16_tflops"] * NOMINAL_RATIO["fp8"],
             "recipe_fp4": peaks["bf16_tflops"] * NOMINAL_RATIO["fp4"],
             "mma_measured_fp8": mma["fp8"] if mma else None, "mma_measured_fp4": mma["fp4"] if mma else None,
-            "used": "recipe (measured bf16 x nominal ratio); the measured MMA rates are reported beside it"},
+            "used": "per format, the larger of the recipe figure and the measured MMA rate"},
         "next": nxt,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": hl["launches"],
         "clocks": hl["clocks"],
     }
+    line["summary"] = summarize(line)  # last, so a tail of the output still shows it
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -6,7 +6,17 @@
 // one 128-byte K atom per group of four MMAs) on operands that stay in shared
 // memory, accumulating in TMEM, with the scale factors already in TMEM: no
 // HBM or L2 traffic, nothing but the tensor pipe.  Each CTA times its loop
-// with %globaltimer from the first issue to the commit's completion.
+// with %globaltimer from the first issue to the commit's completion, and the
+// rate is the whole grid's flops over the span from the earliest start to the
+// latest end (a CTA that ran in a second wave lengthens the span instead of
+// being counted as concurrent).
+//
+// The per-CTA times go through one file-scope device array of at most
+// kP_MaxCtas CTAs, shared by every call: calls must not overlap (two streams
+// or two host threads measuring at once would read each other's times).
+// The kernel allocates all 512 TMEM columns of its SM; tcgen05.alloc waits
+// without a time limit while another resident kernel holds TMEM there, so it
+// is meant for an otherwise idle GPU.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -28,7 +38,8 @@ constexpr int kP_OffBar = 50688;
 // allocation) is resident per SM
 constexpr int kP_Smem = 120 * 1024;
 
-__device__ unsigned long long g_mma_rate_ns[kP_MaxCtas];
+// [2 i]: CTA i's start, [2 i + 1]: its end (%globaltimer, ns); end 0 = its wait gave up
+__device__ unsigned long long g_mma_rate_ns[2 * kP_MaxCtas];
 
 template <int KIND>  // 0: kind::mxf8f6f4 (E4M3 x E4M3), 1: kind::mxf4 (E2M1 x E2M1)
 __global__ void __launch_bounds__(kP_Threads, 1) mma_rate_kernel(int iters, uint64_t limit_ns, unsigned* err) {
@@ -75,7 +86,9 @@ __global__ void __launch_bounds__(kP_Threads, 1) mma_rate_kernel(int iters, uint
         }
         tc_commit(bar);
         const bool ok = mbar_wait(bar, 0, limit_ns, err);
-        g_mma_rate_ns[blockIdx.x] = ok ? globaltimer_ns() - t0 : 0ull;
+        g_mma_rate_ns[2 * blockIdx.x] = t0;
+        g_mma_rate_ns[2 * blockIdx.x + 1] = ok ? globaltimer_ns() : 0ull;
+        if (!ok) mbar_wait(bar, 0, limit_ns, err);  // give the MMAs a second bound before TMEM is freed
     }
     tc_fence_before();
     __syncthreads();
@@ -94,19 +107,21 @@ cudaError_t measure_mma_rate(int kind, int iters, double* tflops, cudaStream_t s
     if (e != cudaSuccess) return e;
     kern<<<grid, kP_Threads, kP_Smem, st>>>(iters, wait_limit_ns(), err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    unsigned long long ns[kP_MaxCtas];
-    if ((e = cudaMemcpyFromSymbolAsync(ns, g_mma_rate_ns, sizeof(unsigned long long) * grid, 0,
+    unsigned long long ns[2 * kP_MaxCtas];
+    if ((e = cudaMemcpyFromSymbolAsync(ns, g_mma_rate_ns, sizeof(unsigned long long) * 2 * grid, 0,
                                        cudaMemcpyDeviceToHost, st)) != cudaSuccess)
         return e;
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return e;
-    unsigned long long worst = 0;
+    unsigned long long first = ~0ull, last = 0;
     for (int i = 0; i < grid; ++i) {
-        if (ns[i] == 0) return cudaErrorLaunchTimeout;  // a CTA's wait gave up
-        worst = std::max(worst, ns[i]);
+        if (ns[2 * i + 1] == 0) return cudaErrorLaunchTimeout;  // a CTA's wait gave up
+        first = std::min(first, ns[2 * i]);
+        last = std::max(last, ns[2 * i + 1]);
     }
+    if (last <= first) return cudaErrorUnknown;
     const double k_per_mma = kind == 1 ? 64.0 : 32.0;
     const double flops = (double)grid * iters * 4 * 2.0 * 128 * 256 * k_per_mma;
-    *tflops = flops / (double)worst / 1e3;
+    *tflops = flops / (double)(last - first) / 1e3;
     return cudaSuccess;
 }
 

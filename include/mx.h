@@ -255,9 +255,13 @@ MX_API mx_status_t mx_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  * One CTA per SM issues `iters` x 4 MMAs of 128 x 256 x (32 E4M3FN or 64
  * E2M1) elements on operands resident in shared memory (fmt selects
  * kind::mxf8f6f4 with E4M3FN x E4M3FN, or kind::mxf4 with E2M1 x E2M1);
- * *tflops receives 2*M*N*K of all MMAs over the slowest CTA's time.
- * Synchronous (waits for `stream`).  iters in 1..1000000 (MX_ERR_SHAPE
- * otherwise); MX_ERR_TIMEOUT if a CTA's bounded wait gave up. */
+ * *tflops receives 2*M*N*K of all MMAs over the span from the first CTA's
+ * start to the last CTA's end.  Synchronous (waits for `stream`).  iters in
+ * 1..1000000 (MX_ERR_SHAPE otherwise); MX_ERR_TIMEOUT if a CTA's bounded wait
+ * gave up.  The per-CTA times pass through one device array (at most 1024
+ * CTAs) that every call shares: calls must not overlap, on any stream or host
+ * thread.  Each CTA allocates all TMEM of its SM, so run it on an otherwise
+ * idle GPU (the allocation waits while another kernel holds TMEM there). */
 MX_API mx_status_t mx_measure_mma_rate(mx_format_t fmt, int iters, double* tflops, void* stream);
 
 /* Static text for a status code. */
