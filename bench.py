@@ -491,6 +491,28 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
             mx.mx_device_status()
             sec_f, dist_f = timed(fused, nsets, steps, 3, world)
     mx.mx_device_status()
+    # the same product with the public row-major scale layout, through the
+    # workspace entry point (its two scale relayout launches timed with it)
+    rm_bytes = lambda rows: mx.mx_scales_bytes(mx.SCALES_ROWMAJOR, rows, K)
+    for s in sets:
+        s["as_rm"] = torch.empty(rm_bytes(M), dtype=torch.uint8, device="cuda")
+        mx.mx_scales_relayout(s["as"], L, M, K, s["as_rm"], mx.SCALES_ROWMAJOR)
+        if "bs_rm" not in s:
+            s["bs_rm"] = torch.empty(rm_bytes(N), dtype=torch.uint8, device="cuda")
+            mx.mx_scales_relayout(s["bs"], L, N, K, s["bs_rm"], mx.SCALES_ROWMAJOR)
+            for t in sets:
+                if t["bs"] is s["bs"]:
+                    t["bs_rm"] = s["bs_rm"]
+    ws = mx.alloc_workspace(M, N, K)
+
+    def gemm_rm(i):
+        s = sets[i]
+        mx.mx_block_matmul_ws(s["ac"], s["as_rm"], fa, s["bc"], s["bs_rm"], fb, M, N, K, s["C"], ws)
+
+    gemm_rm(0)
+    mx.mx_device_status()
+    sec_rm, dist_rm = timed(gemm_rm, nsets, steps, 3, world)
+    mx.mx_device_status()
     flops = 2.0 * M * N * K
     tf_step = job_throughput(flops * steps, world, sec) / 1e12
     tf_gemm = flops * steps / sec_g / 1e12
@@ -508,6 +530,10 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
     if mma is not None:
         out["mma_measured_tflops"] = mma[kind]
         out["tensor_frac_of_mma_measured"] = tf_gemm / mma[kind]
+    out["rowmajor_ws"] = {"what": "row-major scales: mx_block_matmul_ws (one scale relayout launch + the product)",
+                          "us": sec_rm / steps * 1e6, "dist": dist_rm, "tflops": flops * steps / sec_rm / 1e12,
+                          "vs_tensor_core_layout": sec_rm / sec_g, "workspace_bytes": ws.numel() if ws is not None else 0,
+                          "launches_per_step": 2}
     if sec_q is not None:
         g = qa_bytes * steps / sec_q / 1e9
         out["act_quantize"] = {"what": f"{'bf16' if A.dtype == torch.bfloat16 else 'f32'} {M}x{K} -> "
@@ -522,7 +548,7 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
                         "gbs": fused_bytes * steps / sec_f / 1e9,
                         "hbm_frac": fused_bytes * steps / sec_f / 1e9 / peaks["hbm_gbs"], "bytes": fused_bytes,
                         "launches_per_step": 1}
-    del sets, A, C0, bc, bs
+    del sets, A, C0, bc, bs, ws
     torch.cuda.empty_cache()
     if oracle_rows > 0:
         out["oracle"] = oracle_gemm_baseline(w, cfg, a_key, b_key, quant_a, oracle_rows)
@@ -824,6 +850,8 @@ def summarize(line):
             out[key]["act_q_hbm_frac"] = r3(g["act_quantize"]["hbm_frac"])
         if "fused" in g:
             out[key]["fused_us"] = round(g["fused"]["us_per_step"], 1)
+        if "rowmajor_ws" in g:
+            out[key]["rowmajor_ws_us"] = round(g["rowmajor_ws"]["us"], 1)
     return out
 
 

@@ -55,6 +55,10 @@ def _load() -> ctypes.CDLL:
     L.mx_dequantize.restype = i32
     L.mx_block_matmul.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, i64, i64, i64, vp, vp]
     L.mx_block_matmul.restype = i32
+    L.mx_block_matmul_ws.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, i64, i64, i64, vp, vp, i64, vp]
+    L.mx_block_matmul_ws.restype = i32
+    L.mx_block_matmul_workspace_bytes.argtypes = [i32, i64, i64, i64]
+    L.mx_block_matmul_workspace_bytes.restype = i64
     L.mx_scales_relayout.argtypes = [vp, i32, i64, i64, vp, i32, vp]
     L.mx_scales_relayout.restype = i32
     L.mx_quantize_axis.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, i32, vp]
@@ -179,6 +183,45 @@ def mx_block_matmul(a_codes: torch.Tensor, a_scales: torch.Tensor, a_fmt: int,
                                _dev_ptr(b_codes, "b_codes", cb), _dev_ptr(b_scales, "b_scales", sb), b_fmt,
                                scale_layout, block_size, scale_type, M, N, K,
                                _dev_ptr(C, "C", M * N * 4), _stream(stream)))
+
+
+def mx_block_matmul_workspace_bytes(scale_layout: int, M: int, N: int, K: int) -> int:
+    return int(lib.mx_block_matmul_workspace_bytes(scale_layout, M, N, K))
+
+
+def alloc_workspace(M: int, N: int, K: int, scale_layout: int = SCALES_ROWMAJOR) -> torch.Tensor | None:
+    """A device buffer (caller-owned, from torch) for mx_block_matmul_ws; None when none is needed."""
+    n = mx_block_matmul_workspace_bytes(scale_layout, M, N, K)
+    if n < 0:
+        raise ValueError("invalid layout or shape for a block_matmul workspace")
+    return torch.empty(n, dtype=torch.uint8, device="cuda") if n > 0 else None
+
+
+def mx_block_matmul_ws(a_codes: torch.Tensor, a_scales: torch.Tensor, a_fmt: int,
+                       b_codes: torch.Tensor, b_scales: torch.Tensor, b_fmt: int,
+                       M: int, N: int, K: int, C: torch.Tensor, workspace: torch.Tensor | None,
+                       scale_layout: int = SCALES_ROWMAJOR, stream=None,
+                       block_size: int = BLOCK, scale_type: int = SCALE_E8M0) -> None:
+    """mx_block_matmul with a caller-owned workspace: row-major scales are
+    rewritten into it in the tensor-core layout before the product."""
+    need = mx_block_matmul_workspace_bytes(scale_layout, M, N, K) if min(M, N, K) >= 0 else 0
+    ws = _dev_ptr(workspace, "workspace", max(need, 0)) if (workspace is not None and need > 0) else None
+    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if M * N * K == 0:
+        _check(lib.mx_block_matmul_ws(None, None, a_fmt, None, None, b_fmt, scale_layout, block_size, scale_type,
+                                      M, N, K, None, ws, nws, None))
+        return
+    if C.dtype != torch.float32:
+        raise ValueError("C must be float32")
+    ca, cb = mx_codes_bytes(a_fmt, M, K), mx_codes_bytes(b_fmt, N, K)
+    sa, sb = mx_scales_bytes(scale_layout, M, K), mx_scales_bytes(scale_layout, N, K)
+    if min(ca, cb, sa, sb) < 0:
+        _check(lib.mx_block_matmul_ws(None, None, a_fmt, None, None, b_fmt, scale_layout, block_size, scale_type,
+                                      M, N, K, None, ws, nws, None))
+    _check(lib.mx_block_matmul_ws(_dev_ptr(a_codes, "a_codes", ca), _dev_ptr(a_scales, "a_scales", sa), a_fmt,
+                                  _dev_ptr(b_codes, "b_codes", cb), _dev_ptr(b_scales, "b_scales", sb), b_fmt,
+                                  scale_layout, block_size, scale_type, M, N, K,
+                                  _dev_ptr(C, "C", M * N * 4), ws, nws, _stream(stream)))
 
 
 def mx_quantize_axis(x: torch.Tensor, axis: int, fmt: int, codes: torch.Tensor, scales: torch.Tensor,

@@ -314,10 +314,17 @@ mx_status_t mx_measure_mma_rate(mx_format_t fmt, int iters, double* tflops, void
     return ok();
 }
 
-mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
-                            const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
-                            int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,
-                            void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The argument checks of block_matmul (shared by mx_block_matmul and
+// mx_block_matmul_ws).  MX_OK with *empty set: nothing to compute.
+mx_status_t check_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
+                               const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
+                               int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
+                               const float* C, bool* empty) {
+    *empty = false;
     mx_status_t s;
     if ((s = check_common(block_size, scale_type)) != MX_OK) return s;
     if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt)) return fail(MX_ERR_UNSUPPORTED, "element formats %d, %d",
@@ -333,7 +340,10 @@ mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_for
     if (scale_layout == MX_SCALES_ROWMAJOR && K % 128)
         return fail(MX_ERR_SHAPE, "row-major scales need K %% 128 == 0 (K = %lld); use MX_SCALES_MMA",
                     (long long)K);
-    if (M == 0 || N == 0 || K == 0) return ok();  // C += (empty sum) is C
+    if (M == 0 || N == 0 || K == 0) {  // C += (empty sum) is C
+        *empty = true;
+        return MX_OK;
+    }
     if (!a_codes || !a_scales || !b_codes || !b_scales || !C)
         return fail(MX_ERR_NULL, "operand pointers must be non-NULL");
     if (!aligned(a_codes, 16) || !aligned(b_codes, 16) || !aligned(C, 16) || !aligned(a_scales, 16) ||
@@ -347,13 +357,76 @@ mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_for
         overlaps(C, cb, a_scales, mx_scales_bytes(scale_layout, M, K)) ||
         overlaps(C, cb, b_scales, mx_scales_bytes(scale_layout, N, K)))
         return fail(MX_ERR_UNSUPPORTED, "C overlaps an input");
-    if ((s = check_device()) != MX_OK) return s;
-    mx::GemmArgs g{a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, scale_layout, M, N, K, C};
+    return MX_OK;
+}
+
+mx_status_t run_block_matmul(const mx::GemmArgs& g, void* stream) {
     const char* detail = nullptr;
     cudaError_t e = mx::launch_block_matmul(g, static_cast<cudaStream_t>(stream), &detail);
     if (e != cudaSuccess) return fail(MX_ERR_CUDA, "block_matmul: %s%s%s", cudaGetErrorString(e),
                                       detail ? ": " : "", detail ? detail : "");
     return ok();
+}
+
+// Where the tensor-core-layout copy of B's scales starts in a workspace.
+int64_t ws_b_offset(int64_t M, int64_t K) { return mx::round_up(mx_scales_bytes(MX_SCALES_MMA, M, K), 256); }
+
+}  // namespace
+
+extern "C" {
+
+mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
+                            const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
+                            int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,
+                            void* stream) {
+    bool empty;
+    mx_status_t s = check_block_matmul(a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, scale_layout, block_size,
+                                       scale_type, M, N, K, C, &empty);
+    if (s != MX_OK) return s;
+    if (empty) return ok();
+    if ((s = check_device()) != MX_OK) return s;
+    return run_block_matmul({a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, scale_layout, M, N, K, C}, stream);
+}
+
+int64_t mx_block_matmul_workspace_bytes(mx_scale_layout_t scale_layout, int64_t M, int64_t N, int64_t K) {
+    if (!valid_layout(scale_layout) || M < 0 || N < 0 || K < 0 || K % 32) return -1;
+    if (scale_layout == MX_SCALES_MMA || M == 0 || N == 0 || K == 0) return 0;
+    return ws_b_offset(M, K) + mx::round_up(mx_scales_bytes(MX_SCALES_MMA, N, K), 256);
+}
+
+mx_status_t mx_block_matmul_ws(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt, const void* b_codes,
+                               const uint8_t* b_scales, mx_format_t b_fmt, mx_scale_layout_t scale_layout,
+                               int block_size, mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
+                               float* C, void* workspace, int64_t workspace_bytes, void* stream) {
+    bool empty;
+    mx_status_t s = check_block_matmul(a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, scale_layout, block_size,
+                                       scale_type, M, N, K, C, &empty);
+    if (s != MX_OK) return s;
+    if (empty) return ok();
+    if (scale_layout == MX_SCALES_MMA) {
+        if ((s = check_device()) != MX_OK) return s;
+        return run_block_matmul({a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, scale_layout, M, N, K, C},
+                                stream);
+    }
+    const int64_t need = mx_block_matmul_workspace_bytes(scale_layout, M, N, K);
+    if (!workspace) return fail(MX_ERR_NULL, "workspace must be non-NULL for row-major scales");
+    if (workspace_bytes < need)
+        return fail(MX_ERR_SHAPE, "workspace of %lld bytes; these shapes need %lld (mx_block_matmul_workspace_bytes)",
+                    (long long)workspace_bytes, (long long)need);
+    if (!aligned(workspace, 256)) return fail(MX_ERR_ALIGN, "workspace must be 256-byte aligned");
+    if (overlaps(workspace, need, C, M * N * 4) || overlaps(workspace, need, a_codes, mx_codes_bytes(a_fmt, M, K)) ||
+        overlaps(workspace, need, b_codes, mx_codes_bytes(b_fmt, N, K)) ||
+        overlaps(workspace, need, a_scales, mx_scales_bytes(scale_layout, M, K)) ||
+        overlaps(workspace, need, b_scales, mx_scales_bytes(scale_layout, N, K)))
+        return fail(MX_ERR_UNSUPPORTED, "workspace overlaps C or an input");
+    if ((s = check_device()) != MX_OK) return s;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint8_t* a_sf = ws;
+    uint8_t* b_sf = ws + ws_b_offset(M, K);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mx::launch_scales_to_mma(a_scales, M, b_scales, N, K, a_sf, b_sf, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scale relayout launch");
+    return run_block_matmul({a_codes, a_sf, a_fmt, b_codes, b_sf, b_fmt, MX_SCALES_MMA, M, N, K, C}, stream);
 }
 
 mx_status_t mx_scales_relayout(const uint8_t* src, mx_scale_layout_t src_layout, int64_t rows, int64_t cols,

@@ -62,6 +62,11 @@ cudaError_t launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols
                             uint8_t* scales, int layout, cudaStream_t stream);
 cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols, int fmt,
                               int layout, float* y, cudaStream_t stream);
+// Row-major scales of two operands (a_rows and b_rows rows of cols elements,
+// cols % 128 == 0, sources 4-byte aligned) rewritten in the tensor-core
+// layout at a_dst and b_dst (16-byte aligned; padding included), one launch.
+cudaError_t launch_scales_to_mma(const uint8_t* a_src, int64_t a_rows, const uint8_t* b_src, int64_t b_rows,
+                                 int64_t cols, uint8_t* a_dst, uint8_t* b_dst, cudaStream_t st);
 cudaError_t launch_relayout(const uint8_t* src, int src_layout, int64_t rows, int64_t cols, uint8_t* dst,
                             int dst_layout, cudaStream_t stream);
 cudaError_t launch_dequantize_bf16(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols, int fmt,

@@ -466,6 +466,64 @@ __global__ void __launch_bounds__(kThreads) quantize_axis0_kernel(const InT* __r
 
 // ------------------------------------------------------------------ relayout
 
+// Row-major scales [rows][nb] (nb % 4 == 0) -> the tensor-core layout, as
+// 32-bit words: row r's word g (blocks 4g .. 4g+3) goes to word
+// 4 (r % 32) + (r / 32) % 4 of tile (r / 128, g).  Both operands of a product
+// in one launch: a CTA takes 128 rows and kRmGroups words of them of one
+// operand through shared memory, reading whole rows (16-byte loads when rows
+// are 16-byte multiples) and writing whole 512-byte tiles (16-byte stores);
+// rows past the end are written as zero padding.
+constexpr int kRmGroups = 32;
+
+struct RmOperand {
+    const uint32_t* src;
+    uint32_t* dst;
+    int64_t rows;
+    int64_t ctas;  // tiles x group chunks
+};
+
+__global__ void __launch_bounds__(256) scales_to_mma_kernel(RmOperand a, RmOperand b, int64_t ng, int64_t gchunks) {
+    __shared__ uint32_t tile[128][kRmGroups + 1];
+    pdl_launch_dependents();
+    int64_t cta = blockIdx.x;
+    const bool is_a = cta < a.ctas;
+    if (!is_a) cta -= a.ctas;
+    const uint32_t* __restrict__ src = is_a ? a.src : b.src;
+    uint32_t* __restrict__ dst = is_a ? a.dst : b.dst;
+    const int64_t rows = is_a ? a.rows : b.rows;
+    const int64_t t = cta / gchunks;
+    const int64_t r0 = t * 128, g0 = (cta - t * gchunks) * kRmGroups;
+    const int gn = (int)(ng - g0 < kRmGroups ? ng - g0 : kRmGroups);
+    pdl_wait();
+    if ((ng & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        // gn is a multiple of 4 here: whole 16-byte quads of each row
+        for (int i = threadIdx.x; i < 128 * (kRmGroups / 4); i += blockDim.x) {
+            const int r = i / (kRmGroups / 4), q = i % (kRmGroups / 4);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (4 * q < gn && r0 + r < rows)
+                v = *reinterpret_cast<const uint4*>(src + (r0 + r) * ng + g0 + 4 * q);
+            tile[r][4 * q] = v.x;
+            tile[r][4 * q + 1] = v.y;
+            tile[r][4 * q + 2] = v.z;
+            tile[r][4 * q + 3] = v.w;
+        }
+    } else {
+        for (int i = threadIdx.x; i < 128 * kRmGroups; i += blockDim.x) {
+            const int r = i / kRmGroups, g = i % kRmGroups;
+            uint32_t v = 0;
+            if (g < gn && r0 + r < rows) v = src[(r0 + r) * ng + g0 + g];
+            tile[r][g] = v;
+        }
+    }
+    __syncthreads();
+    // output word 4k + j of a tile holds row 32 j + k
+    for (int i = threadIdx.x; i < 32 * gn; i += blockDim.x) {
+        const int g = i / 32, k = i % 32;
+        *reinterpret_cast<uint4*>(dst + (t * ng + g0 + g) * 128 + 4 * k) =
+            make_uint4(tile[k][g], tile[32 + k][g], tile[64 + k][g], tile[96 + k][g]);
+    }
+}
+
 __global__ void relayout_kernel(const uint8_t* __restrict__ src, int src_layout, int64_t rows, int64_t nb,
                                 uint8_t* __restrict__ dst, int dst_layout) {
     const int64_t nb4 = round_up(nb, 4);
@@ -641,6 +699,18 @@ cudaError_t launch_quantize_axis0(const void* x, int dtype, int64_t rows, int64_
     // two columns per 32-bit load when every row starts on a 4-byte boundary
     if ((cols & 1) == 0) return axis0_fmt<__nv_bfloat16, 2>(p, rows, cols, fmt, c, scales, layout, st);
     return axis0_fmt<__nv_bfloat16, 1>(p, rows, cols, fmt, c, scales, layout, st);
+}
+
+cudaError_t launch_scales_to_mma(const uint8_t* a_src, int64_t a_rows, const uint8_t* b_src, int64_t b_rows,
+                                 int64_t cols, uint8_t* a_dst, uint8_t* b_dst, cudaStream_t st) {
+    const int64_t ng = cols / 128;  // 4-block words per row
+    if (ng == 0 || (a_rows == 0 && b_rows == 0)) return cudaSuccess;
+    const int64_t gchunks = (ng + kRmGroups - 1) / kRmGroups;
+    RmOperand a{reinterpret_cast<const uint32_t*>(a_src), reinterpret_cast<uint32_t*>(a_dst), a_rows,
+                (a_rows + 127) / 128 * gchunks};
+    RmOperand b{reinterpret_cast<const uint32_t*>(b_src), reinterpret_cast<uint32_t*>(b_dst), b_rows,
+                (b_rows + 127) / 128 * gchunks};
+    return launch_pdl(scales_to_mma_kernel, dim3((unsigned)(a.ctas + b.ctas)), dim3(256), 0, st, a, b, ng, gchunks);
 }
 
 cudaError_t launch_relayout(const uint8_t* src, int src_layout, int64_t rows, int64_t cols, uint8_t* dst,

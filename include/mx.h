@@ -153,6 +153,35 @@ MX_API mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales,
                             mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K,
                             float* C, void* stream);
 
+/* block_matmul with a caller-owned device workspace ([Dialect] "The four ops",
+ * "The block axis", "The accumulator operand"; the workspace, like every
+ * buffer here, is the caller's: destination passing).  Arguments and result
+ * as mx_block_matmul.  With MX_SCALES_MMA the workspace is unused (may be
+ * NULL) and the call is mx_block_matmul.  With MX_SCALES_ROWMAJOR (K % 128 ==
+ * 0) both operands' scales are first rewritten into the workspace in the
+ * tensor-core layout -- A's at byte 0, B's at the next 256-byte boundary --
+ * by one small kernel on `stream`, and the product then runs as with
+ * MX_SCALES_MMA (the row-major path of mx_block_matmul gathers scale words
+ * inside the GEMM and is slower).  The workspace is only written; its
+ * previous contents do not matter.
+ *   workspace       : device pointer, 256-byte aligned (MX_ERR_ALIGN), not
+ *                     overlapping C or an input (MX_ERR_UNSUPPORTED).
+ *   workspace_bytes : at least mx_block_matmul_workspace_bytes(...)
+ *                     (MX_ERR_SHAPE otherwise; MX_ERR_NULL for a NULL
+ *                     workspace that row-major scales need).
+ * Asynchronous on `stream`; the workspace must stay allocated until the call
+ * has run, and two calls that share a workspace must be ordered. */
+MX_API mx_status_t mx_block_matmul_ws(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt,
+                               const void* b_codes, const uint8_t* b_scales, mx_format_t b_fmt,
+                               mx_scale_layout_t scale_layout, int block_size, mx_scale_type_t scale_type,
+                               int64_t M, int64_t N, int64_t K, float* C, void* workspace,
+                               int64_t workspace_bytes, void* stream);
+
+/* Bytes of workspace mx_block_matmul_ws needs: 0 for MX_SCALES_MMA or an empty
+ * product; for MX_SCALES_ROWMAJOR the tensor-core-layout scale bytes of A and
+ * of B, each rounded up to 256.  -1 for an invalid layout or shape. */
+MX_API int64_t mx_block_matmul_workspace_bytes(mx_scale_layout_t scale_layout, int64_t M, int64_t N, int64_t K);
+
 /* quantize_block along an explicit block axis ([Dialect] "The block axis":
  * blocks run along the reduction axis, which for the right-hand operand of a
  * product is its first axis).

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 16
+    assert len(names) == 18
     out = subprocess.run(["nm", "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (mx_\w+)", out))
     for n in names:
@@ -113,6 +113,31 @@ def test_block_matmul_validation():
     assert g(C=A16) == UNSUP                    # C overlaps A's codes
     assert g(layout=mx.SCALES_ROWMAJOR, K=96) == SHAPE   # row-major scales need K % 128 == 0
     assert g(M=0) == OK and g(N=0) == OK and g(K=0) == OK
+
+
+def gw(ws=A16 * 256, nws=1 << 20, layout=mx.SCALES_ROWMAJOR, M=4, N=4, K=128, C=A16 * 64):
+    return L.mx_block_matmul_ws(A16, A16 * 2, mx.E2M1, A16 * 3, A16 * 5, mx.E2M1, layout, 32, 1, M, N, K, C, ws,
+                                nws, None)
+
+
+def test_block_matmul_workspace_bytes_and_validation():
+    need = L.mx_block_matmul_workspace_bytes
+    # row-major scales: the tensor-core-layout scale bytes of A and B, each rounded up to 256
+    rnd = lambda v: (v + 255) // 256 * 256
+    for M, N, K in ((4, 4, 128), (130, 300, 1024), (8192, 28672, 8192), (16, 14336, 4096)):
+        assert need(mx.SCALES_ROWMAJOR, M, N, K) == rnd(mx.mx_scales_bytes(mx.SCALES_MMA, M, K)) + \
+            rnd(mx.mx_scales_bytes(mx.SCALES_MMA, N, K))
+    assert need(mx.SCALES_MMA, 4, 4, 128) == 0
+    assert need(mx.SCALES_ROWMAJOR, 0, 4, 128) == 0
+    assert need(mx.SCALES_ROWMAJOR, 4, 4, 48) == -1
+    assert need(5, 4, 4, 128) == -1
+    # checks that run before anything is launched
+    assert gw(ws=None) == NULL
+    assert gw(nws=need(mx.SCALES_ROWMAJOR, 4, 4, 128) - 1) == SHAPE
+    assert gw(ws=A16 * 256 + 16) == ALIGN
+    assert gw(ws=A16 * 64) == UNSUP          # overlaps C
+    assert gw(K=96) == SHAPE                 # row-major scales need K % 128 == 0
+    assert gw(M=0) == OK
 
 
 def test_relayout_and_selftest_validation():
