@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
     L.mx_block_matmul_ws.restype = i32
     L.mx_block_matmul_workspace_bytes.argtypes = [i32, i64, i64, i64]
     L.mx_block_matmul_workspace_bytes.restype = i64
+    L.mx_block_matmul_static_ws.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, i64, i64, i64, vp, vp]
+    L.mx_block_matmul_static_ws.restype = i32
     L.mx_scales_relayout.argtypes = [vp, i32, i64, i64, vp, i32, vp]
     L.mx_scales_relayout.restype = i32
     L.mx_quantize_axis.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, i32, vp]

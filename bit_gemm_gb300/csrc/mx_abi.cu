@@ -100,6 +100,11 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
 
 }  // namespace
 
+namespace mx {
+// For entry points defined in other files: a failure with its detail text.
+mx_status_t record_failure(mx_status_t s, const char* detail) { return fail(s, "%s", detail); }
+}  // namespace mx
+
 extern "C" {
 
 int64_t mx_codes_bytes(mx_format_t fmt, int64_t rows, int64_t cols) {

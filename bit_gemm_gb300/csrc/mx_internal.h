@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "mx.h"
+
 #include <mutex>
 #include <set>
 #include <utility>
@@ -62,6 +64,10 @@ cudaError_t launch_quantize(const void* x, int dtype, int64_t rows, int64_t cols
                             uint8_t* scales, int layout, cudaStream_t stream);
 cudaError_t launch_dequantize(const void* codes, const uint8_t* scales, int64_t rows, int64_t cols, int fmt,
                               int layout, float* y, cudaStream_t stream);
+// Sets the detail text mx_last_error_detail() returns and returns s (for
+// entry points defined outside mx_abi.cu).
+mx_status_t record_failure(mx_status_t s, const char* detail);
+
 // Row-major scales of two operands (a_rows and b_rows rows of cols elements,
 // cols % 128 == 0, sources 4-byte aligned) rewritten in the tensor-core
 // layout at a_dst and b_dst (16-byte aligned; padding included), one launch.

@@ -182,6 +182,33 @@ MX_API mx_status_t mx_block_matmul_ws(const void* a_codes, const uint8_t* a_scal
  * of B, each rounded up to 256.  -1 for an invalid layout or shape. */
 MX_API int64_t mx_block_matmul_workspace_bytes(mx_scale_layout_t scale_layout, int64_t M, int64_t N, int64_t K);
 
+/* mx_block_matmul_ws for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is a deployment variant.  Callers in this
+ * position include a host framework or plugin runtime that owns every device
+ * buffer and hands a library only its inputs and outputs, a process held to a
+ * device memory budget fixed at start-up, and latency-critical code where an
+ * allocation, which may synchronize the device, is not acceptable.
+ * Arguments and result are those of mx_block_matmul; the caller still passes
+ * every input and C.  The scratch for the tensor-core-layout scales is one
+ * file-scope device array of 16 MiB (16777216 bytes), which every GPU that
+ * loads the library holds until the process exits, so products whose
+ * mx_block_matmul_workspace_bytes exceed that are rejected with MX_ERR_SHAPE
+ * (for example M = N = K = 8192 needs 4 MiB, M = 8192, N = 28672, K = 8192
+ * needs 9 MiB).  The call allocates nothing: no cudaMalloc, cudaFree or other
+ * allocating routine.
+ * Every call shares that one array, which keeps the last call's contents; a
+ * call rewrites every byte it reads, so nothing needs clearing, but calls that
+ * overlap on the GPU (other streams, or host threads without ordering between
+ * their calls) race on it and can produce wrong results.  The first call on a
+ * device looks up the array's device address (set-up, once per device) and
+ * should come before any stream capture.  With MX_SCALES_MMA no scratch is
+ * used and the call is mx_block_matmul. */
+MX_API mx_status_t mx_block_matmul_static_ws(const void* a_codes, const uint8_t* a_scales, mx_format_t a_fmt,
+                                      const void* b_codes, const uint8_t* b_scales, mx_format_t b_fmt,
+                                      mx_scale_layout_t scale_layout, int block_size,
+                                      mx_scale_type_t scale_type, int64_t M, int64_t N, int64_t K, float* C,
+                                      void* stream);
+
 /* quantize_block along an explicit block axis ([Dialect] "The block axis":
  * blocks run along the reduction axis, which for the right-hand operand of a
  * product is its first axis).
