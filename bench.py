@@ -688,19 +688,33 @@ def traffic_case(mx, launches):
             "dequantize_algorithmic_bytes": d}
 
 
+def headline_kernel_digest() -> str:
+    """sha256 of the source the headline kernels are built from: the sections
+    of mx_quant.cu from its top through the dequantize kernel (loads, the
+    quantize kernels, the dequantize decoders and kernel), and the device
+    headers they include.  Other kernels in the same file do not change it."""
+    import hashlib
+    csrc = os.path.join(ROOT, "bit_gemm_gb300", "csrc")
+    with open(os.path.join(csrc, "mx_quant.cu")) as f:
+        text = f.read()
+    end = text.index("// ---------------------------------------------------------------- fold_scale")
+    h = hashlib.sha256(text[:end].encode())
+    for name in ("mx_quant_block.cuh", "mx_device.cuh", "mx_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def measured_traffic(key: str):
     """DRAM bytes per launch from the committed ncu capture, or None when the
-    kernel source has changed since the counters were taken."""
-    import hashlib
+    headline kernels' source has changed since the counters were taken."""
     prof = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "bit_gemm_gb300", "csrc", "mx_quant.cu")
     if not os.path.exists(prof):
         return None
     with open(prof) as f:
         d = json.load(f)
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != d.get("mx_quant_cu_sha256"):
-            return None
+    if headline_kernel_digest() != d.get("headline_kernel_sha256"):
+        return None
     return d.get(key)
 
 
