@@ -80,6 +80,9 @@ cudaError_t launch_dequantize_bf16(const void* codes, const uint8_t* scales, int
 cudaError_t launch_fold_scale(uint8_t* scales, int64_t rows, int64_t cols, int layout, int j, cudaStream_t stream);
 // x [rows][cols] blocked along rows; codes/scales in the layout of the [cols][rows] transpose.
 // The same through shared-memory tiles (TMA); applies when x and its rows start on 16-byte boundaries.
+bool quantize_axis0_direct_applies(const void* x, int dtype, int64_t cols, const void* codes);
+cudaError_t launch_quantize_axis0_direct(const void* x, int64_t rows, int64_t cols, int fmt, void* codes,
+                                         uint8_t* scales, int layout, cudaStream_t st);
 bool quantize_axis0_tiled_applies(const void* x, int dtype, int64_t cols);
 cudaError_t launch_quantize_axis0_tiled(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, void* codes,
                                         uint8_t* scales, int layout, cudaStream_t stream);

@@ -739,6 +739,8 @@ cudaError_t axis0_fmt(const InT* x, int64_t rows, int64_t cols, int fmt, uint8_t
 
 cudaError_t launch_quantize_axis0(const void* x, int dtype, int64_t rows, int64_t cols, int fmt, void* codes,
                                   uint8_t* scales, int layout, cudaStream_t st) {
+    if (quantize_axis0_direct_applies(x, dtype, cols, codes))
+        return launch_quantize_axis0_direct(x, rows, cols, fmt, codes, scales, layout, st);
     if (quantize_axis0_tiled_applies(x, dtype, cols))
         return launch_quantize_axis0_tiled(x, dtype, rows, cols, fmt, codes, scales, layout, st);
     uint8_t* c = static_cast<uint8_t*>(codes);

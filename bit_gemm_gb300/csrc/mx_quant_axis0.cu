@@ -210,7 +210,130 @@ cudaError_t axis0_dispatch(const CUtensorMap& tx, const CUtensorMap& tc, const A
                                 : run_axis0<InT, FMT_E4M3, LAYOUT_ROWMAJOR>(tx, tc, p, st);
 }
 
+// ------------------------------------------------- bf16: loads straight to registers
+//
+// For bf16 input the units above leave an SM with eight quantizing warps (the
+// staged tiles fill its shared memory), too few to cover the latency of their
+// column walks.  Here nothing is staged and an SM holds many small CTAs: a CTA
+// of four warps takes 64 columns x 4 blocks (128 rows), warp w block w and
+// lane l columns 2l and 2l + 1.  A lane loads its 32 rows as 32-bit words (a
+// warp's load is one 128-byte row segment), rounds both columns from those
+// words with the scale and rounding of the row-wise bf16 path, and writes
+// each column's codes of the block with one 32-byte (E4M3) or 16-byte (E2M1)
+// store; the CTA's four warps together write whole 128- or 64-byte runs of
+// each column.  The scale bytes meet in shared memory and leave as one 32-bit
+// word per column (blocks 4 ry .. 4 ry + 3).
+constexpr int kXD_Threads = 128;
+
+// kP column pairs per lane (1: 32-bit loads; 2: 64-bit loads, cols % 4 == 0)
+template <int FMT, int LAYOUT, int kP>
+__global__ void __launch_bounds__(kXD_Threads, kP == 1 ? 8 : 5)
+    quantize_axis0_direct_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t nb,
+                                 int64_t ncx, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    constexpr int kOut = FMT == FMT_E2M1 ? 4 : 8;
+    constexpr int kCols = 64 * kP;      // columns per CTA
+    __shared__ uint32_t s_word[kCols];  // scale word of each of the CTA's columns, block w in byte w
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ry = blockIdx.x / ncx, cx = blockIdx.x - ry * ncx;
+    const int64_t blk = 4 * ry + warp;
+    const int64_t c = kCols * cx + 2 * kP * lane;  // the lane's first column; cols % (2 kP) == 0
+    pdl_wait();                                    // the previous kernel's writes are visible
+    uint32_t sbytes[kP];                           // zero: padding past nb or cols
+#pragma unroll
+    for (int q = 0; q < kP; ++q) sbytes[q] = 0;
+    if (blk < nb && c < cols) {
+        const __nv_bfloat16* p = x + 32 * blk * cols + c;
+        uint32_t w[kP][32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if constexpr (kP == 1) {
+                w[0][i] = __ldcs(reinterpret_cast<const unsigned int*>(p + i * cols));
+            } else {
+                const uint2 v = __ldcs(reinterpret_cast<const uint2*>(p + i * cols));
+                w[0][i] = v.x;
+                w[1][i] = v.y;
+            }
+        }
+        const int64_t code_row = FMT == FMT_E2M1 ? rows / 2 : rows;
+        uint8_t* dst = codes + c * code_row + (FMT == FMT_E2M1 ? 16 : 32) * blk;
+#pragma unroll
+        for (int q = 0; q < kP; ++q) {
+            uint32_t out[2][kOut];
+            sbytes[q] = quantize_column_pair_bf16<FMT>(w[q], out[0], out[1]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint8_t* d = dst + (2 * q + h) * code_row;
+                if constexpr (FMT == FMT_E2M1) {
+                    *reinterpret_cast<uint4*>(d) = make_uint4(out[h][0], out[h][1], out[h][2], out[h][3]);
+                } else {
+                    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d), "r"(out[h][0]),
+                                 "r"(out[h][1]), "r"(out[h][2]), "r"(out[h][3]), "r"(out[h][4]), "r"(out[h][5]),
+                                 "r"(out[h][6]), "r"(out[h][7])
+                                 : "memory");
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kP; ++q) {
+        reinterpret_cast<uint8_t*>(s_word)[(2 * kP * lane + 2 * q) * 4 + warp] = (uint8_t)sbytes[q];
+        reinterpret_cast<uint8_t*>(s_word)[(2 * kP * lane + 2 * q + 1) * 4 + warp] = (uint8_t)(sbytes[q] >> 8);
+    }
+    __syncthreads();
+    if (threadIdx.x < kCols) {
+        const int64_t col = kCols * cx + threadIdx.x;
+        const uint32_t word = s_word[threadIdx.x];
+        if (LAYOUT == LAYOUT_MMA) {
+            // the grid covers the layout's padding columns (to a multiple of 128)
+            const int t = (int)(col & 127);
+            uint32_t* tile = reinterpret_cast<uint32_t*>(scales + ((col >> 7) * (round_up(nb, 4) >> 2) + ry) * 512);
+            tile[(t & 31) * 4 + (t >> 5)] = word;
+        } else if (col < cols) {
+            uint8_t* d = scales + col * nb + 4 * ry;
+            const int nblk = (int)min((int64_t)4, nb - 4 * ry);
+            if (nblk == 4 && (nb & 3) == 0) {
+                *reinterpret_cast<uint32_t*>(d) = word;
+            } else {
+                for (int b = 0; b < nblk; ++b) d[b] = (uint8_t)(word >> (8 * b));
+            }
+        }
+    }
+}
+
+template <int FMT, int kP>
+cudaError_t run_axis0_direct(const __nv_bfloat16* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* scales,
+                             int layout, cudaStream_t st) {
+    const int64_t nb = rows / 32;
+    // the tensor-core layout's grid covers its padding columns, to a multiple of 128
+    const int64_t ncx = layout == LAYOUT_MMA ? (128 / (64 * kP)) * ((cols + 127) / 128) : (cols + 64 * kP - 1) / (64 * kP);
+    const int64_t ctas = ncx * ((nb + 3) / 4);
+    if (ctas == 0) return cudaSuccess;
+    const dim3 grid((unsigned)ctas), block(kXD_Threads);
+    if (layout == LAYOUT_MMA)
+        return launch_pdl(quantize_axis0_direct_kernel<FMT, LAYOUT_MMA, kP>, grid, block, 0, st, x, rows, cols, nb, ncx, codes, scales);
+    return launch_pdl(quantize_axis0_direct_kernel<FMT, LAYOUT_ROWMAJOR, kP>, grid, block, 0, st, x, rows, cols, nb, ncx, codes, scales);
+}
+
 }  // namespace
+
+bool quantize_axis0_direct_applies(const void* x, int dtype, int64_t cols, const void* codes) {
+    return dtype != DT_F32 && (cols & 1) == 0 && (reinterpret_cast<uintptr_t>(x) & 3) == 0 &&
+           (reinterpret_cast<uintptr_t>(codes) & 31) == 0;
+}
+
+cudaError_t launch_quantize_axis0_direct(const void* x, int64_t rows, int64_t cols, int fmt, void* codes,
+                                         uint8_t* scales, int layout, cudaStream_t st) {
+    const __nv_bfloat16* xp = static_cast<const __nv_bfloat16*>(x);
+    uint8_t* cp = static_cast<uint8_t*>(codes);
+    // 64-bit loads when every row starts on an 8-byte boundary
+    const bool wide = (cols & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0;
+    if (fmt == FMT_E2M1)
+        return wide ? run_axis0_direct<FMT_E2M1, 2>(xp, rows, cols, cp, scales, layout, st)
+                    : run_axis0_direct<FMT_E2M1, 1>(xp, rows, cols, cp, scales, layout, st);
+    return wide ? run_axis0_direct<FMT_E4M3, 2>(xp, rows, cols, cp, scales, layout, st)
+                : run_axis0_direct<FMT_E4M3, 1>(xp, rows, cols, cp, scales, layout, st);
+}
 
 bool quantize_axis0_tiled_applies(const void* x, int dtype, int64_t cols) {
     const int64_t row_bytes = cols * (dtype == DT_F32 ? 4 : 2);

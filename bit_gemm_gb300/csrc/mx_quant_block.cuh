@@ -168,20 +168,26 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&a)[8]) {
     return r;
 }
 
-// Quantize one block of 32 bf16 (16 words, low half = lower element).
-// Returns the scale byte; fills 32 bytes (E4M3FN) or 16 bytes (E2M1) of codes.
+// The larger magnitude in each bf16 half of a and b, one instruction: with
+// the sign bits cleared afterwards, the result is the larger |x| of the two
+// when both are numbers (the bit patterns of non-negative bf16 values order
+// as the values do), the infinity when one is infinite, and the canonical NaN
+// 0x7FFF when either is a NaN -- so a block's maximum over these is below
+// 0x7F80 exactly when the block holds no NaN or infinity, and then equals the
+// largest magnitude's bits.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The scale of a bf16 block from m, the bf16 bits of its largest magnitude
+// (sign cleared), and below 0x7F80 (no NaN or infinity, which poison the
+// block: scale byte 0xFF, codes 0).  Returns the scale byte e + 127 and sets
+// c = 2^-e (1 - 2^-12), the multiplier that pre-scales the block's elements.
 template <int FMT>
-__device__ __forceinline__ uint32_t quantize_block_bf16(const uint32_t (&w)[16], uint32_t (&out)[FMT == FMT_E2M1 ? 4 : 8]) {
+__device__ __forceinline__ uint32_t bf16_block_scale(uint32_t m, float& c) {
     constexpr int kEmax = FMT == FMT_E2M1 ? 2 : 8;
-    uint32_t m2 = w[0] & 0x7FFF7FFFu;
-#pragma unroll
-    for (int i = 1; i < 16; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
-    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);  // bf16 bits of the block's amax
-    if (m >= 0x7F80u) {  // NaN or infinity in the block: poison it
-#pragma unroll
-        for (int i = 0; i < (FMT == FMT_E2M1 ? 4 : 8); ++i) out[i] = 0;
-        return 0xFFu;
-    }
     // floor(log2 amax) from the bits: normal 2^(field-127), subnormal m * 2^-133
     const int fe = (int)(m >> 7);
     const int E = fe ? fe - 127 : (31 - __clz((int)m)) - 133;
@@ -189,7 +195,26 @@ __device__ __forceinline__ uint32_t quantize_block_bf16(const uint32_t (&w)[16],
     e = e < -127 ? -127 : (e > 127 ? 127 : e);
     e = m ? e : 0;  // all-zero block: scale byte 127, codes +0
     // 2^-e * (1 - 2^-12) = 2^(-e-1) * (2 - 2^-11)
-    const float c = __uint_as_float(((uint32_t)(126 - e) << 23) | 0x7FF000u);
+    c = __uint_as_float(((uint32_t)(126 - e) << 23) | 0x7FF000u);
+    return (uint32_t)(e + 127);
+}
+
+// Quantize one block of 32 bf16 (16 words, low half = lower element).
+// Returns the scale byte; fills 32 bytes (E4M3FN) or 16 bytes (E2M1) of codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_block_bf16(const uint32_t (&w)[16], uint32_t (&out)[FMT == FMT_E2M1 ? 4 : 8]) {
+    uint32_t m2 = w[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) m2 = bf16x2_absmax(m2, w[i]);
+    m2 &= 0x7FFF7FFFu;
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);  // bf16 bits of the block's amax
+    if (m >= 0x7F80u) {  // NaN or infinity in the block: poison it
+#pragma unroll
+        for (int i = 0; i < (FMT == FMT_E2M1 ? 4 : 8); ++i) out[i] = 0;
+        return 0xFFu;
+    }
+    float c;
+    const uint32_t sbyte = bf16_block_scale<FMT>(m, c);
     float y[32];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -207,7 +232,54 @@ __device__ __forceinline__ uint32_t quantize_block_bf16(const uint32_t (&w)[16],
 #pragma unroll
         for (int k = 0; k < 8; ++k) out[k] = cvt_e4m3x4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
     }
-    return (uint32_t)(e + 127);
+    return sbyte;
+}
+
+// Quantize the blocks of two neighbouring columns at once: w[i] holds row i
+// of column 0 in its low half and of column 1 in its high half (one 32-bit
+// load of a bf16 row).  The same scale and rounding as quantize_block_bf16.
+// Returns the two scale bytes (column 1 in bits 8..15); fills each column's
+// codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_column_pair_bf16(const uint32_t (&w)[32],
+                                                              uint32_t (&out0)[FMT == FMT_E2M1 ? 4 : 8],
+                                                              uint32_t (&out1)[FMT == FMT_E2M1 ? 4 : 8]) {
+    constexpr int kOut = FMT == FMT_E2M1 ? 4 : 8;
+    uint32_t m2 = w[0];
+#pragma unroll
+    for (int i = 1; i < 32; ++i) m2 = bf16x2_absmax(m2, w[i]);
+    m2 &= 0x7FFF7FFFu;
+    uint32_t sbytes = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t(&out)[kOut] = h ? out1 : out0;
+        const uint32_t m = h ? m2 >> 16 : m2 & 0xFFFFu;
+        uint32_t sbyte = 0xFFu;
+        if (m >= 0x7F80u) {  // NaN or infinity in the block: poison it
+#pragma unroll
+            for (int i = 0; i < kOut; ++i) out[i] = 0;
+        } else {
+            float c;
+            sbyte = bf16_block_scale<FMT>(m, c);
+            float y[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                y[i] = __fmaf_rn(__uint_as_float(h ? w[i] & 0xFFFF0000u : w[i] << 16), c, 0.0f);
+            if (FMT == FMT_E2M1) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float a[8] = {y[8 * k], y[8 * k + 1], y[8 * k + 2], y[8 * k + 3],
+                                        y[8 * k + 4], y[8 * k + 5], y[8 * k + 6], y[8 * k + 7]};
+                    out[k] = cvt_e2m1x8(a);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) out[k] = cvt_e4m3x4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+            }
+        }
+        sbytes |= sbyte << (8 * h);
+    }
+    return sbytes;
 }
 
 // Quantize one block of 32 elements given as binary32 bit patterns (bf16 inputs

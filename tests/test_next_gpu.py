@@ -67,8 +67,10 @@ def test_axis0_shapes(fmt, dtype, layout):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("layout", [mx.SCALES_ROWMAJOR, mx.SCALES_MMA])
 def test_axis0_tiled_shapes(fmt, dtype, layout):
-    # rows of 16-byte multiples take the shared-memory tile path: ragged last
-    # column tiles (264, 520, 1000 columns), one block row, many units per CTA
+    # rows of 16-byte multiples: f32 takes the shared-memory tile kernel, bf16
+    # the register kernel (four columns per lane when the column count is a
+    # multiple of 4, else two); ragged last column tiles (264, 520, 1000
+    # columns), one block row, many units per CTA
     rng = np.random.default_rng(13)
     for rows, cols in [(32, 8), (64, 264), (96, 520), (1024, 1000), (2048, 4096)]:
         x = torch.from_numpy(rand(rng, (rows, cols))).to(dtype)
