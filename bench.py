@@ -531,9 +531,16 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
         s = sets[i]
         mx.mx_block_matmul_ws(s["ac"], s["as_rm"], fa, s["bc"], s["bs_rm"], fb, M, N, K, s["C"], ws)
 
+    def gemm_rm_direct(i):
+        s = sets[i]
+        mx.mx_block_matmul(s["ac"], s["as_rm"], fa, s["bc"], s["bs_rm"], fb, M, N, K, s["C"], mx.SCALES_ROWMAJOR)
+
     gemm_rm(0)
     mx.mx_device_status()
     sec_rm, dist_rm = timed(gemm_rm, nsets, steps, 3, world)
+    gemm_rm_direct(0)
+    mx.mx_device_status()
+    sec_rmd, dist_rmd = timed(gemm_rm_direct, nsets, steps, 3, world)
     mx.mx_device_status()
     flops = 2.0 * M * N * K
     tf_step = job_throughput(flops * steps, world, sec) / 1e12
@@ -556,6 +563,9 @@ def bench_gemm(mx, cfg, steps, warmup, world, peaks, scale=1.0, dev_index=0, mma
                           "us": sec_rm / steps * 1e6, "dist": dist_rm, "tflops": flops * steps / sec_rm / 1e12,
                           "vs_tensor_core_layout": sec_rm / sec_g, "workspace_bytes": ws.numel() if ws is not None else 0,
                           "launches_per_step": 2}
+    out["rowmajor_direct"] = {"what": "row-major scales: mx_block_matmul (scales gathered inside the product)",
+                              "us": sec_rmd / steps * 1e6, "dist": dist_rmd, "tflops": flops * steps / sec_rmd / 1e12,
+                              "vs_tensor_core_layout": sec_rmd / sec_g, "launches_per_step": 1}
     if sec_q is not None:
         g = qa_bytes * steps / sec_q / 1e9
         out["act_quantize"] = {"what": f"{'bf16' if A.dtype == torch.bfloat16 else 'f32'} {M}x{K} -> "
@@ -888,6 +898,8 @@ def summarize(line):
             out[key]["fused_us"] = round(g["fused"]["us_per_step"], 1)
         if "rowmajor_ws" in g:
             out[key]["rowmajor_ws_us"] = round(g["rowmajor_ws"]["us"], 1)
+        if "rowmajor_direct" in g:
+            out[key]["rowmajor_direct_us"] = round(g["rowmajor_direct"]["us"], 1)
     return out
 
 

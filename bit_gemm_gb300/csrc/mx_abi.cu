@@ -425,6 +425,10 @@ mx_status_t mx_block_matmul_ws(const void* a_codes, const uint8_t* a_scales, mx_
         overlaps(workspace, need, b_scales, mx_scales_bytes(scale_layout, N, K)))
         return fail(MX_ERR_UNSUPPORTED, "workspace overlaps C or an input");
     if ((s = check_device()) != MX_OK) return s;
+    if (mx::block_matmul_gathers_scales_fast(a_fmt, b_fmt, M, N, K))
+        // decode shapes: the product reads the row-major scales itself, one launch
+        return run_block_matmul({a_codes, a_scales, a_fmt, b_codes, b_scales, b_fmt, scale_layout, M, N, K, C},
+                                stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint8_t* a_sf = ws;
     uint8_t* b_sf = ws + ws_b_offset(M, K);

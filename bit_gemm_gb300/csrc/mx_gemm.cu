@@ -475,6 +475,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         const uint32_t lstep = li == 0 ? C_::A_BYTES : li == 1 ? C_::B_BYTES : li == 2 ? C_::SFA_BYTES : C_::SFB_BYTES;
         uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
         int fills = 0;
+        // row-major scales: the lane's scale rows of the current tile, and their byte counts
+        const uint8_t* rm_a[4];
+        const uint8_t* rm_b[C_::SFB_TILES][4];
+        uint32_t rm_na[4], rm_nb[C_::SFB_TILES][4];
         uint32_t issued_phase = 0;
         bool ok = true;
         Work w;
@@ -498,8 +502,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 }
                 // scale groups present for this stage (the last stage of a
                 // ragged K may need only the first)
-                const int g_first = (kb + p.k_atom0) * C_::G;
-                const int g_count = min(C_::G, p.sf_groups - g_first);
+                const int g_first = (kb + p.k_atom0) * C_::GS;
+                const int g_count = min(C_::GS, p.sf_groups - g_first);
                 // A stage is A, B and (tensor-core scale layout) the scale boxes
                 // of both, issued by lanes 0..3 with one instruction where the
                 // operand maps are 3-D; boxes past the tensor's end read zeros
@@ -520,22 +524,35 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     __syncwarp();
                 }
                 if (p.sf_rowmajor) {
-                    for (int g = 0; g < g_count; ++g) {
-                        const int64_t word = 4 * (int64_t)(g_first + g);  // byte offset of the group in a row
-                        uint8_t* da = smem + C_::OFF_SFA + stage * C_::SFA_BYTES + g * 512 + lane * 16;
+                    if (j == 0) {
+                        // this lane's scale rows of the tile: A rows p0 + lane + 32 i, B rows
+                        // q0 + 128 t + lane + 32 i (rows past the end read nothing, as zeros)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int32_t r = p0 + lane + 32 * i;
-                            const int32_t rc = r < p.P ? r : p.P - 1;
-                            cp_async_4(da + 4 * i, p.sfa + (int64_t)rc * p.nb + word, r < p.P ? 4u : 0u);
+                            rm_a[i] = p.sfa + (int64_t)(r < p.P ? r : p.P - 1) * p.nb;
+                            rm_na[i] = r < p.P ? 4u : 0u;
+#pragma unroll
+                            for (int t = 0; t < C_::SFB_TILES; ++t) {
+                                const int32_t rb = q0 + 128 * t + lane + 32 * i;
+                                rm_b[t][i] = p.sfb + (int64_t)(rb < p.Q ? rb : p.Q - 1) * p.nb;
+                                rm_nb[t][i] = rb < p.Q ? 4u : 0u;
+                            }
                         }
+                    }
+                    for (int g = 0; g < g_count; ++g) {
+                        const int word = 4 * (g_first + g);  // byte offset of the group in a row
+                        uint8_t* da = smem + C_::OFF_SFA + stage * C_::SFA_BYTES + g * 512 + lane * 16;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) cp_async_4(da + 4 * i, rm_a[i] + word, rm_na[i]);
+#pragma unroll
                         for (int t = 0; t < C_::SFB_TILES; ++t) {
-                            uint8_t* db = smem + C_::OFF_SFB + stage * C_::SFB_BYTES + (t * C_::G + g) * 512 + lane * 16;
+                            // group g of row tile t where the MMA side reads it
+                            uint8_t* db = smem + C_::OFF_SFB + stage * C_::SFB_BYTES + (t * C_::GS + g) * 512 + lane * 16;
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const int32_t r = q0 + 128 * t + lane + 32 * i;
-                                const int32_t rc = r < p.Q ? r : p.Q - 1;
-                                cp_async_4(db + 4 * i, p.sfb + (int64_t)rc * p.nb + word, r < p.Q ? 4u : 0u);
+                                // the MMA reads the first BN rows of B's scale tiles only
+                                if (128 * t + 32 * i < BN) cp_async_4(db + 4 * i, rm_b[t][i] + word, rm_nb[t][i]);
                             }
                         }
                     }
@@ -1617,6 +1634,15 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
 
 }  // namespace
 
+bool block_matmul_gathers_scales_fast(int a_fmt, int b_fmt, int64_t M, int64_t N, int64_t K) {
+    // the swapped one-CTA kernel with two K atoms per stage (the condition on
+    // `sa` in launch_block_matmul): its producer gathers row-major scale words
+    // into the tensor-core tiles at about the cost of the bulk scale copies
+    const bool swap = M <= 64 && N > M;
+    const int64_t k_per_stage = (a_fmt == FMT_E2M1 && b_fmt == FMT_E2M1) ? 256 : 128;
+    return swap && round_up(M, 16) <= 32 && K % (2 * k_per_stage) == 0;
+}
+
 cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char** detail) {
     *detail = nullptr;
     const bool swap = a.M <= 64 && a.N > a.M;
@@ -1649,8 +1675,8 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     CUtensorMap ta, tb, tsa, tsb, tc;
     const int op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
     // decode shapes stream two K atoms per stage when K allows (the stage
-    // count, not the bytes, bounds them)
-    const int sa = (swap && bn <= 32 && a.scale_layout == LAYOUT_MMA && a.K % (2 * k_per_stage) == 0) ? 2 : 1;
+    // count, not the bytes, bounds them), with either scale layout
+    const int sa = (swap && bn <= 32 && a.K % (2 * k_per_stage) == 0) ? 2 : 1;
     auto opmap = [&](CUtensorMap* m, const void* codes, int64_t rows, int f, int box_rows) {
         return op3d ? make_operand_map3n(m, codes, rows, a.K, fk(f), box_rows, sa)
                     : make_operand_map(m, codes, rows, a.K, fk(f), box_rows);

@@ -102,6 +102,10 @@ struct GemmArgs {
 };
 // Returns cudaSuccess or an error; *detail gets a static explanation on failure.
 cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t stream, const char** detail);
+// True when block_matmul on row-major scales runs at about the speed of the
+// tensor-core layout (decode shapes: at most 32 rows of A, K a whole number of
+// two-atom stages), so a scale relayout in front of it would only add a launch.
+bool block_matmul_gathers_scales_fast(int a_fmt, int b_fmt, int64_t M, int64_t N, int64_t K);
 
 struct GemmActArgs {
     const void* act;  // [M][K] f32 or bf16

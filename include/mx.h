@@ -162,8 +162,12 @@ MX_API mx_status_t mx_block_matmul(const void* a_codes, const uint8_t* a_scales,
  * tensor-core layout -- A's at byte 0, B's at the next 256-byte boundary --
  * by one small kernel on `stream`, and the product then runs as with
  * MX_SCALES_MMA (the row-major path of mx_block_matmul gathers scale words
- * inside the GEMM and is slower).  The workspace is only written; its
- * previous contents do not matter.
+ * inside the GEMM and is slower for most shapes).  The exception is decode
+ * shapes -- M <= 32 with N > M, and K a multiple of 256 (512 when both
+ * operands are MX_E2M1) -- where the gather costs about what the bulk scale
+ * copies do: those calls are mx_block_matmul with row-major scales and leave
+ * the workspace untouched (it is still validated).  The workspace is only
+ * written; its previous contents do not matter.
  *   workspace       : device pointer, 256-byte aligned (MX_ERR_ALIGN), not
  *                     overlapping C or an input (MX_ERR_UNSUPPORTED).
  *   workspace_bytes : at least mx_block_matmul_workspace_bytes(...)

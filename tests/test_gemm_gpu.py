@@ -172,7 +172,11 @@ def test_two_atom_stages(M, N, K, fa, fb):
     (128, 128, 256, mx.E2M1, mx.E2M1),
     (200, 300, 384, mx.E4M3FN, mx.E4M3FN),   # ragged M and N: scale rows past the end read as zero
     (130, 512, 128, mx.E4M3FN, mx.E2M1),
-    (16, 1024, 512, mx.E4M3FN, mx.E2M1),     # swapped operands
+    (16, 1024, 512, mx.E4M3FN, mx.E2M1),     # swapped operands, two K atoms per stage
+    (16, 1040, 4096, mx.E4M3FN, mx.E2M1),    # decode shape, ragged weight rows, split along K
+    (5, 300, 1024, mx.E4M3FN, mx.E4M3FN),    # fewer activation rows than a scale tile
+    (32, 264, 1024, mx.E2M1, mx.E2M1),       # FP4, two scale groups per atom, 32 activation rows
+    (48, 520, 1024, mx.E2M1, mx.E4M3FN),     # 48 activation rows: one-atom stages
     (256, 512, 8192, mx.E2M1, mx.E2M1),      # split along K across CTAs
 ])
 def test_row_major_scales(M, N, K, fa, fb):
@@ -185,6 +189,12 @@ def test_row_major_scales(M, N, K, fa, fb):
 def test_workload3_decode_full():
     w = workloads.make(3)
     run_full(w["A"], w["W"], mx.E4M3FN, mx.E2M1, w["C0"])
+
+
+def test_workload3_decode_full_row_major_scales():
+    # the public scale layout, gathered by the producer lanes (two K atoms per stage)
+    w = workloads.make(3)
+    run_full(w["A"], w["W"], mx.E4M3FN, mx.E2M1, w["C0"], layout=mx.SCALES_ROWMAJOR)
 
 
 # --------------------------------------------- workloads 4 and 5, sampled

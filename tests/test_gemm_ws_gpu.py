@@ -22,6 +22,12 @@ from test_gemm_gpu import O_FMT, check, gpu_quant, host_f32, randn
 pytestmark = pytest.mark.gpu
 
 
+def gathers_scales(M, N, K, fa, fb):
+    """Decode shapes, which mx_block_matmul_ws runs on the row-major scales directly."""
+    k_stage = 256 if (fa == mx.E2M1 and fb == mx.E2M1) else 128
+    return M <= 64 and N > M and -(-M // 16) * 16 <= 32 and K % (2 * k_stage) == 0
+
+
 def run_ws(A, Bt, fa, fb, C0, canary=True):
     M, K = A.shape
     N = Bt.shape[0]
@@ -36,16 +42,21 @@ def run_ws(A, Bt, fa, fb, C0, canary=True):
     mx.mx_device_status()
     if canary:
         assert (to_np(ws_full[need:]) == 0xA5).all(), "bytes past the workspace were written"
-    # (1) the workspace holds both operands' scales in the tensor-core layout
     oa, osa = oracle.quantize(host_f32(A), O_FMT[fa])
     ob, osb = oracle.quantize(host_f32(Bt), O_FMT[fb])
-    nb = K // 32
-    sa_mma = rowmajor_to_mma(osa, M, nb)
-    sb_mma = rowmajor_to_mma(osb, N, nb)
-    off_b = (sa_mma.size + 255) // 256 * 256
     w = to_np(ws)
-    assert np.array_equal(w[:sa_mma.size], sa_mma), "A scales in the workspace"
-    assert np.array_equal(w[off_b:off_b + sb_mma.size], sb_mma), "B scales in the workspace"
+    if gathers_scales(M, N, K, fa, fb):
+        # (1') decode shapes read the row-major scales in the product: the
+        # workspace is left as it was
+        assert (w == 0xA5).all(), "decode shapes leave the workspace untouched"
+    else:
+        # (1) the workspace holds both operands' scales in the tensor-core layout
+        nb = K // 32
+        sa_mma = rowmajor_to_mma(osa, M, nb)
+        sb_mma = rowmajor_to_mma(osb, N, nb)
+        off_b = (sa_mma.size + 255) // 256 * 256
+        assert np.array_equal(w[:sa_mma.size], sa_mma), "A scales in the workspace"
+        assert np.array_equal(w[off_b:off_b + sb_mma.size], sb_mma), "B scales in the workspace"
     # (2) the product against the oracle
     ref, sabs = oracle.block_matmul(oa, osa, O_FMT[fa], ob, osb, O_FMT[fb], M, N, K, C0)
     check(to_np(C), ref, sabs, C0, f"ws {M}x{N}x{K} {fa}x{fb}")
@@ -65,7 +76,9 @@ def run_ws(A, Bt, fa, fb, C0, canary=True):
     (200, 72, 512, mx.E4M3FN, mx.E2M1),        # mixed formats
     (520, 776, 1024, mx.E2M1, mx.E2M1),       # CTA pairs, ragged
     (640, 520, 2048, mx.E4M3FN, mx.E4M3FN),    # CTA pairs, two K atoms per stage
-    (16, 1040, 4096, mx.E4M3FN, mx.E2M1),      # decode shape (operands swapped), split along K
+    (16, 1040, 4096, mx.E4M3FN, mx.E2M1),      # decode shape: the product gathers the scales itself
+    (32, 520, 1024, mx.E2M1, mx.E2M1),        # decode shape, FP4, 32 activation rows
+    (48, 300, 1024, mx.E4M3FN, mx.E4M3FN),     # 48 rows: relayout, then the product
     (5, 300, 128, mx.E4M3FN, mx.E4M3FN),       # fewer rows than a scale tile
 ])
 def test_rowmajor_through_workspace(M, N, K, fa, fb):
