@@ -1675,8 +1675,9 @@ cudaError_t launch_block_matmul(const GemmArgs& a, cudaStream_t st, const char**
     CUtensorMap ta, tb, tsa, tsb, tc;
     const int op3d = (a.K % k_per_stage) == 0 ? 1 : 0;
     // decode shapes stream two K atoms per stage when K allows (the stage
-    // count, not the bytes, bounds them), with either scale layout
-    const int sa = (swap && bn <= 32 && a.K % (2 * k_per_stage) == 0) ? 2 : 1;
+    // count, not the bytes, bounds them), with either scale layout; the same
+    // rule tells mx_block_matmul_ws which shapes need no scale relayout
+    const int sa = block_matmul_gathers_scales_fast(a.a_fmt, a.b_fmt, a.M, a.N, a.K) ? 2 : 1;
     auto opmap = [&](CUtensorMap* m, const void* codes, int64_t rows, int f, int box_rows) {
         return op3d ? make_operand_map3n(m, codes, rows, a.K, fk(f), box_rows, sa)
                     : make_operand_map(m, codes, rows, a.K, fk(f), box_rows);

@@ -1,23 +1,28 @@
-// mx_quant_axis0.cu -- quantize with the blocks along the first axis, through
-// shared memory.
+// mx_quant_axis0.cu -- quantize with the blocks along the first axis.
 //
 // "Block-scaled matmul in MLIR" ([Dialect] "The block axis"): the blocks of a
 // K x N right-hand operand run down its columns (along K), and its codes and
 // scales are stored in the layout of the N x K transpose, ready to be the
-// block_matmul operand.  Reading a column block straight from HBM means 32
-// strided loads per block, and writing each block's codes on its own means
-// 16- or 32-byte pieces scattered one per output row.  This kernel works on
-// units of [128 rows x 128 columns]: TMA brings the tile into shared memory,
-// thread c quantizes column c (four blocks, with the rounding of the last-axis
-// quantize), the 128 columns' codes -- one whole 128-byte (E4M3FN) or 64-byte
-// (E2M1) run of each output row -- are staged in shared memory and leave with
-// one TMA tensor store, and the scales leave as one 32-bit word per column
-// (in the tensor-core layout a unit's scales are one contiguous 512-byte
-// tile, padding included).
+// block_matmul operand.  Two kernels:
 //
-// Persistent CTAs, two per SM for bf16 input: warp 0 streams input tiles
-// through a ring of stages; warps 1..4 quantize.  Units (column tile, row
-// group), row group fastest, are dealt to CTAs as contiguous ranges.
+// * bf16 input (even column count): loads straight to registers.  A CTA of
+//   four warps takes 128 (or 64) columns x 4 blocks; a lane loads its 32 rows
+//   of four (or two) neighbouring columns as 64-bit (or 32-bit) words, one
+//   row segment per warp load, rounds each column's block with the row-wise
+//   bf16 routine's arithmetic, and writes each column's codes of the block
+//   with one 32-byte (E4M3FN) or 16-byte (E2M1) store; the scale words meet
+//   in shared memory.  Many small CTAs per SM keep the loads in flight.
+//
+// * f32 input: units of [128 rows x 128 columns] through shared memory.  TMA
+//   brings the tile in, thread c quantizes column c (four blocks, with the
+//   rounding of the last-axis quantize), the 128 columns' codes -- one whole
+//   128-byte (E4M3FN) or 64-byte (E2M1) run of each output row -- are staged
+//   in shared memory and leave with one TMA tensor store, and the scales leave
+//   as one 32-bit word per column (in the tensor-core layout a unit's scales
+//   are one contiguous 512-byte tile, padding included).  Persistent CTAs:
+//   warp 0 streams input tiles through a ring of stages; warps 1..4
+//   quantize; units (column tile, row group), row group fastest, are dealt to
+//   CTAs as contiguous ranges.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

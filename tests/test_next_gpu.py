@@ -24,21 +24,27 @@ def rand(rng, shape, spread=25):
     return x
 
 
-def axis0_gpu(x: torch.Tensor, fmt: int, layout: int):
+def axis0_gpu(x: torch.Tensor, fmt: int, layout: int, codes_offset: int = 0):
+    """codes_offset: start the codes this many bytes into their buffer (16 puts
+    them on a 16- but not a 32-byte boundary, which the register kernel for
+    bf16 input does not take)."""
     rows, cols = x.shape
     cb, sb = mx.mx_codes_bytes(fmt, cols, rows), mx.mx_scales_bytes(layout, cols, rows)
-    codes = torch.full((cb + GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+    codes_buf = torch.full((codes_offset + cb + GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+    codes = codes_buf[codes_offset:]
     scales = torch.full((sb + GUARD,), 0x5A, dtype=torch.uint8, device="cuda")
     mx.mx_quantize_axis(x.cuda(), 0, fmt, codes, scales, layout)
     mx.mx_device_status()
-    c, s = to_np(codes), to_np(scales)
+    c, s = to_np(codes_buf), to_np(scales)
+    assert (c[:codes_offset] == 0xA5).all(), "wrote before the codes"
+    c = c[codes_offset:]
     assert (c[cb:] == 0xA5).all() and (s[sb:] == 0x5A).all(), "wrote past the end"
     return c[:cb], s[:sb]
 
 
-def check_axis0(x: torch.Tensor, fmt: int, layout: int):
+def check_axis0(x: torch.Tensor, fmt: int, layout: int, codes_offset: int = 0):
     rows, cols = x.shape
-    codes, scales = axis0_gpu(x, fmt, layout)
+    codes, scales = axis0_gpu(x, fmt, layout, codes_offset)
     oc, os_ = oracle.quantize_axis0(x.float().numpy(), O_FMT[fmt])
     assert np.array_equal(codes.reshape(oc.shape), oc), "codes differ from the oracle"
     nb = rows // 32
@@ -75,6 +81,17 @@ def test_axis0_tiled_shapes(fmt, dtype, layout):
     for rows, cols in [(32, 8), (64, 264), (96, 520), (1024, 1000), (2048, 4096)]:
         x = torch.from_numpy(rand(rng, (rows, cols))).to(dtype)
         check_axis0(x, fmt, layout)
+
+
+@pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
+@pytest.mark.parametrize("layout", [mx.SCALES_ROWMAJOR, mx.SCALES_MMA])
+def test_axis0_bf16_codes_off_32_bytes(fmt, layout):
+    # bf16 input with codes on a 16- but not a 32-byte boundary takes the
+    # shared-memory tile kernel instead of the register one
+    rng = np.random.default_rng(17)
+    for rows, cols in [(64, 264), (1024, 1000)]:
+        x = torch.from_numpy(rand(rng, (rows, cols))).to(torch.bfloat16)
+        check_axis0(x, fmt, layout, codes_offset=16)
 
 
 @pytest.mark.parametrize("fmt", [mx.E2M1, mx.E4M3FN])
