@@ -981,13 +981,20 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
 // stages fit, and a third less data crosses from L2 per MMA.
 // SA: K atoms per stage (a stage is then one 3-D box of SA atoms per operand
 // and scale tensor: the per-stage issue cost is paid once per SA atoms).
-template <int KIND, int STAGES, int EC = 16, int SA = 1>
+// MMA-issuing warps of the two-atom pair configurations
+constexpr int kPairMW = 2;
+
+// MW: MMA-issuing warps (1, or 2 with two-atom stages: warp 1 issues atom 0
+// of every stage, the warp after the gate atom 1, both into the one
+// accumulator)
+template <int KIND, int STAGES, int EC = 16, int SA = 1, int MW = 1>
 struct PairCfg {
     static constexpr int G = KIND == KIND_F4 ? 2 : 1;  // scale groups per atom
     static constexpr int GS = SA * G;                   // scale groups per stage
     static constexpr int EPI_WARPS = 8;
-    static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp
-    static constexpr int THREADS = 32 * (GATE_WARP + 1);
+    static constexpr int GATE_WARP = 2 + EPI_WARPS;  // waits on stage barriers for the MMA warp(s)
+    static constexpr int THREADS = 32 * (GATE_WARP + MW);
+    static constexpr int TILE_BAR = STAGES + 1;      // named barrier of the MMA warps' tile hand-off
     static constexpr int A_ATOM = 128 * kRowBytes;
     static constexpr int B_ATOM = 128 * kRowBytes;
     static constexpr int A_BYTES = SA * A_ATOM;
@@ -1006,20 +1013,22 @@ struct PairCfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUF;
-    static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16;
+    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
     static constexpr uint32_t SF_TX = (uint32_t)(SFA_BYTES + SFB_BYTES);
+    static_assert(MW == 1 || (MW == 2 && SA == 2), "two MMA warps take one atom of a two-atom stage each");
+    static_assert(TILE_BAR <= 15, "named barrier ids");
     static_assert(SF_SLOTS >= 2, "at least two scale slots in TMEM");
     static_assert(SMEM <= 232448, "shared memory per CTA");
     static_assert(STAGES <= 15, "one named barrier per stage");
 };
 
-template <int KIND, int STAGES, int EC = 16, int SA = 1>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES, EC, SA>::THREADS, 1)
+template <int KIND, int STAGES, int EC = 16, int SA = 1, int MW = 1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES, EC, SA, MW>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                      const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    using C_ = PairCfg<KIND, STAGES, EC, SA>;
+    using C_ = PairCfg<KIND, STAGES, EC, SA, MW>;
     extern __shared__ uint8_t smem_raw[];
     // the same offsets in both CTAs: the MMAs and barrier addresses rely on it
     // aligned by an offset from the array itself: the compiler then keeps the
@@ -1029,8 +1038,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
     uint64_t* empty = full + STAGES;
     uint64_t* tmem_full = empty + STAGES;
     uint64_t* tmem_empty = tmem_full + 1;  // used in the even CTA
-    uint64_t* mma_done = tmem_empty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* mma_done = tmem_empty + 1;  // [2], one per MMA warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -1044,11 +1053,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], MW);  // one commit per MMA warp
         }
-        mbar_init(tmem_full, 1);
+        mbar_init(tmem_full, MW);
         mbar_init(tmem_empty, 2 * C_::EPI_WARPS);
-        mbar_init(mma_done, 1);
+        mbar_init(&mma_done[0], 1);
+        mbar_init(&mma_done[1], 1);
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_a);
@@ -1127,13 +1137,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || (MW > 1 && warp == C_::GATE_WARP + 1)) {
         // ---------------------------------------------------------- MMA issue
         // The whole warp walks the schedule and syncs on stage s's named
         // barrier (1 + s) with the gate warp; lane 0 issues.  After an abort
         // the warp keeps walking (and syncing) without issuing, so its syncs
-        // and the gate's always pair up.
+        // and the gate's always pair up.  With two MMA warps, warp m issues
+        // atom m of every stage (its scale copies, four MMAs, a commit) into
+        // the one accumulator; the first MMA of a work unit, which overwrites
+        // the accumulator, is warp 0's, and warp 1 issues nothing of that unit
+        // until warp 0 has (a tcgen05 fence and the tile hand-off barrier, once
+        // per unit), after which the order of the two warps' MMAs only changes
+        // the rounding order of the sums.
         if (rank == 0) {
+            const int m = warp == 1 ? 0 : 1;
+            constexpr int AW = SA / MW;  // atoms per MMA warp
+            const int a_first = m * AW;
             const uint64_t a_desc0 = smem_desc(smem_u32(smem + C_::OFF_A), 0, 1024, 2);
             const uint64_t b_desc0 = smem_desc(smem_u32(smem + C_::OFF_B), 0, 1024, 2);
             const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C_::OFF_SFA), 0, 128, 0);
@@ -1161,7 +1180,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                     if (lane == 0) *abort_flag = 1;
                 }
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    named_bar_sync(1 + stage, 64);  // the gate saw this stage's data land
+                    named_bar_sync(1 + stage, 32 * (1 + MW));  // the gate saw this stage's data land
+                    if (MW > 1 && m == 1 && kb == w.kb0) named_bar_sync(C_::TILE_BAR, 64);  // see above
                     if (lane == 0 && live) {
                         tc_fence_after();
                         const uint32_t sf_col = tmem + C_::SF_COL0 + sf_slot * C_::SF_COLS_STAGE;
@@ -1173,7 +1193,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                         // at sf_col + SF_COLS_A + 4 (2g + t); g counts the stage's groups
                         // (atom a holds groups a G ..)
 #pragma unroll
-                        for (int g = 0; g < C_::GS; ++g) {
+                        for (int gg = 0; gg < AW * C_::G; ++gg) {
+                            const int g = a_first * C_::G + gg;  // this warp's atoms' groups
                             tc_cp_pair_32x128b_warpx4(sf_col + 4 * g, sfa_desc + g * 32);
 #pragma unroll
                             for (int t = 0; t < 2; ++t)
@@ -1183,7 +1204,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                         const int rem = p.K - kb * k_elem_per_stage;
                         if (SA > 1 || rem >= k_elem_per_stage) {
 #pragma unroll
-                            for (int a = 0; a < SA; ++a) {
+                            for (int aa = 0; aa < AW; ++aa) {
+                                const int a = a_first + aa;
                                 const uint64_t ad = a_desc + a * (C_::A_ATOM >> 4);
                                 const uint64_t bd = b_desc + a * (C_::B_ATOM >> 4);
 #pragma unroll
@@ -1217,6 +1239,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                         tc_commit_pair(&empty[stage]);  // stage free in both CTAs once read
                     }
                     __syncwarp();
+                    if (MW > 1 && m == 0 && kb == w.kb0) {
+                        // hand-off: warp 1's MMAs of this unit come after the one that overwrote
+                        if (lane == 0) tc_fence_before();
+                        named_bar_sync(C_::TILE_BAR, 64);
+                    }
                     if (++sf_slot == C_::SF_SLOTS) sf_slot = 0;
                     if (++stage == STAGES) stage = 0;
                 }
@@ -1224,9 +1251,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                 __syncwarp();
             }
             if (lane == 0) {
-                // every tcgen05 op issued for the pair completes before TMEM is freed
-                tc_commit_pair(mma_done);
-                mbar_wait(mma_done, 0, p.wait_limit_ns, err);
+                // every tcgen05 op this thread issued completes before TMEM is freed
+                tc_commit_pair(&mma_done[m]);
+                mbar_wait(&mma_done[m], 0, p.wait_limit_ns, err);
             }
             __syncwarp();
         }
@@ -1255,7 +1282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                             if (lane == 0) *abort_flag = 1;
                         }
                     }
-                    named_bar_sync(1 + stage, 64);
+                    named_bar_sync(1 + stage, 32 * (1 + MW));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -1489,19 +1516,19 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 
 // CTA pairs that can be resident at once for a pair-kernel instantiation
 // (pairs need two SMs of one GPU processing cluster); cached per instantiation.
-template <int KIND, int STAGES, int EC = 16, int SA = 1>
+template <int KIND, int STAGES, int EC = 16, int SA = 1, int MW = 1>
 cudaError_t run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                      const CUtensorMap& tc, const GemmParams& p, int pairs, cudaStream_t st) {
-    using C_ = PairCfg<KIND, STAGES, EC, SA>;
-    auto kern = gemm_pair_kernel<KIND, STAGES, EC, SA>;
+    using C_ = PairCfg<KIND, STAGES, EC, SA, MW>;
+    auto kern = gemm_pair_kernel<KIND, STAGES, EC, SA, MW>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(2 * pairs), dim3(C_::THREADS), C_::SMEM, st, ta, tb, tsa, tsb, tc, p);
 }
 
-template <int KIND, int STAGES, int EC = 16, int SA = 1>
+template <int KIND, int STAGES, int EC = 16, int SA = 1, int MW = 1>
 int pair_capacity() {
-    using C_ = PairCfg<KIND, STAGES, EC, SA>;
+    using C_ = PairCfg<KIND, STAGES, EC, SA, MW>;
     static std::mutex mu;
     static int cap[64];
     static bool known[64];
@@ -1512,7 +1539,7 @@ int pair_capacity() {
     }
     std::lock_guard<std::mutex> lock(mu);
     if (known[dev]) return cap[dev];
-    auto kern = gemm_pair_kernel<KIND, STAGES, EC, SA>;
+    auto kern = gemm_pair_kernel<KIND, STAGES, EC, SA, MW>;
     int n = 0;
     if (ensure_smem_limit(reinterpret_cast<const void*>(kern), C_::SMEM) == cudaSuccess) {
         cudaLaunchConfig_t cfg;
@@ -1573,8 +1600,9 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
     // through 32 x 8 boxes (1 KB per warp) to make room.
     const int64_t k_atom = kind == KIND_F4 ? 256 : 128;
     const int sa = (a.K % (2 * k_atom)) == 0 ? 2 : 1;
-    const int cap = kind == KIND_F4 ? (sa == 2 ? pair_capacity<KIND_F4, 3, 8, 2>() : pair_capacity<KIND_F4, 6, 8>())
-                                    : (sa == 2 ? pair_capacity<KIND_F8F6F4, 3, 16, 2>() : pair_capacity<KIND_F8F6F4, 6>());
+    const int cap = kind == KIND_F4 ? (sa == 2 ? pair_capacity<KIND_F4, 3, 8, 2, kPairMW>() : pair_capacity<KIND_F4, 6, 8>())
+                                    : (sa == 2 ? pair_capacity<KIND_F8F6F4, 3, 16, 2, kPairMW>()
+                                               : pair_capacity<KIND_F8F6F4, 6>());
     if (cap <= 0) return cudaErrorNotSupported;
     const int64_t k_per_stage = sa * k_atom;
     const int g = sa * (kind == KIND_F4 ? 2 : 1);
@@ -1625,8 +1653,8 @@ cudaError_t launch_pair(const GemmArgs& a, int kind, const void* x_codes, const 
         pairs = (int)(p.total_units < cap ? p.total_units : cap);
     }
     if (sa == 2) {
-        if (kind == KIND_F4) return run_pair<KIND_F4, 3, 8, 2>(ta, tb, tsa, tsb, tc, p, pairs, st);
-        return run_pair<KIND_F8F6F4, 3, 16, 2>(ta, tb, tsa, tsb, tc, p, pairs, st);
+        if (kind == KIND_F4) return run_pair<KIND_F4, 3, 8, 2, kPairMW>(ta, tb, tsa, tsb, tc, p, pairs, st);
+        return run_pair<KIND_F8F6F4, 3, 16, 2, kPairMW>(ta, tb, tsa, tsb, tc, p, pairs, st);
     }
     if (kind == KIND_F4) return run_pair<KIND_F4, 6, 8>(ta, tb, tsa, tsb, tc, p, pairs, st);
     return run_pair<KIND_F8F6F4, 6>(ta, tb, tsa, tsb, tc, p, pairs, st);
