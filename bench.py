@@ -915,7 +915,7 @@ def main():
     ap.add_argument("--only", choices=["headline", "decode", "square", "prefill", "next", "traffic"], default=None,
                     help="run one workload only, print its numbers and exit (profiling runs)")
     ap.add_argument("--scale", type=float, default=1.0,
-                    help="row-count scale of the GEMM workloads with --only (1 = full size)")
+                    help="scale of M and N of the GEMM workloads with --only (1 = full size)")
     ap.add_argument("--oracle-rows", type=int, default=16,
                     help="rows of A in the CPU oracle's timed block_matmul sample (workloads 4 and 5)")
     args = ap.parse_args()
