@@ -984,6 +984,63 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
 // MMA-issuing warps of the two-atom pair configurations
 constexpr int kPairMW = 2;
 
+// Waits that end a launch after an abort -- for loads and MMAs already
+// issued, which always complete -- use at least this limit, whatever limit
+// the caller set for the waits that can give up.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+
+// Named barrier `id` over `count` threads that also ORs a predicate across
+// them: returns whether any participant passed true (no shared-memory access).
+__device__ __forceinline__ bool named_bar_red_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Count `bytes` as arrived on the current phase of a barrier of this CTA.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// A 32-bit store into the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// After the pair kernel's loop, in the even CTA (one thread, after a cluster
+// barrier that made the odd CTA's fill count visible): every load either CTA
+// issued has landed when this returns (or the drain limit has passed).
+//  - A fill is issued by a producer only after its wait on the slot's empty
+//    barrier saw the MMAs of the slot's previous fill complete, which needed
+//    that fill's full phase, armed by the even CTA and fed by both CTAs'
+//    loads.  So the two fill counts differ by at most STAGES, no slot has two
+//    fills that only one CTA issued, and when such a fill f is adjusted its
+//    slot's barrier is in f's phase.
+//  - A fill the even CTA issued (and armed with both CTAs' bytes) and the odd
+//    CTA did not: the odd CTA's bytes are counted as arrived.  A fill only the
+//    odd CTA issued: the even CTA arms it with the odd CTA's bytes.
+//  - Then each slot's last fill is waited for (the slot's earlier fills were
+//    consumed before it was issued, so its phase parity is unambiguous).
+template <int STAGES>
+__device__ void drain_pair_loads(uint64_t* full, int n_even, int n_odd, uint32_t one_cta_tx, uint64_t limit,
+                                 unsigned* err) {
+    const int lo = n_even < n_odd ? n_even : n_odd;
+    const int hi = n_even < n_odd ? n_odd : n_even;
+    for (int f = lo; f < hi; ++f) {
+        if (f < n_even) mbar_complete_tx(&full[f % STAGES], one_cta_tx);
+        else mbar_arrive_expect_tx(&full[f % STAGES], one_cta_tx);
+    }
+    for (int s = 0; s < STAGES && s < hi; ++s) {
+        const int last = s + ((hi - 1 - s) / STAGES) * STAGES;
+        mbar_wait(&full[s], (uint32_t)(last / STAGES) & 1u, limit, err);
+    }
+}
+
 // MW: MMA-issuing warps (1, or 2 with two-atom stages: warp 1 issues atom 0
 // of every stage, the warp after the gate atom 1, both into the one
 // accumulator)
@@ -1041,6 +1098,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
     uint64_t* mma_done = tmem_empty + 1;  // [2], one per MMA warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint32_t* fills = tmem_slot + 2;  // [0]: this CTA's fills issued; [1] (even CTA): the odd CTA's
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1093,6 +1151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
+        uint32_t n_fill = 0;  // fills issued
         Work w;
         for (int it = 0; ok && get_work(p, pair, npairs, it, w); ++it) {
             const int32_t a_row = w.tp * 256 + (int32_t)rank * 128;
@@ -1122,19 +1181,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                     else if (lane < 4) tma_load_3d_pair_at(dst, lmap, 0, y, z, bar);
                 }
                 __syncwarp();
+                ++n_fill;
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
         }
-        if (!ok && lane == 0) {
-            // loads already issued count on the even CTA's barriers, which
-            // this CTA cannot wait on: give them time to land before the
-            // CTA may leave
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 100000) {
-            }
+        // the fill count goes to the even CTA, which waits at the end for every
+        // load of both CTAs (this CTA's loads count on its barriers)
+        if (lane == 0) {
+            if (rank == 0) fills[0] = n_fill;
+            else st_shared_cluster_u32(mapa_shared(smem_u32(&fills[1]), 0), n_fill);
         }
         __syncwarp();
     } else if (warp == 1 || (MW > 1 && warp == C_::GATE_WARP + 1)) {
@@ -1180,7 +1238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                     if (lane == 0) *abort_flag = 1;
                 }
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    named_bar_sync(1 + stage, 32 * (1 + MW));  // the gate saw this stage's data land
+                    // the gate saw this stage's data land, or gave up waiting for it
+                    if (named_bar_red_or(1 + stage, 32 * (1 + MW), false)) live = false;
                     if (MW > 1 && m == 1 && kb == w.kb0) named_bar_sync(C_::TILE_BAR, 64);  // see above
                     if (lane == 0 && live) {
                         tc_fence_after();
@@ -1253,7 +1312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
             if (lane == 0) {
                 // every tcgen05 op this thread issued completes before TMEM is freed
                 tc_commit_pair(&mma_done[m]);
-                mbar_wait(&mma_done[m], 0, p.wait_limit_ns, err);
+                mbar_wait(&mma_done[m], 0, p.wait_limit_ns > kDrainLimitNs ? p.wait_limit_ns : kDrainLimitNs, err);
             }
             __syncwarp();
         }
@@ -1282,7 +1341,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
                             if (lane == 0) *abort_flag = 1;
                         }
                     }
-                    named_bar_sync(1 + stage, 32 * (1 + MW));
+                    // the MMA warps learn here whether this stage's data landed: after
+                    // a give-up they issue nothing more, so a slot is only released
+                    // (and refilled) once its data has landed
+                    named_bar_red_or(1 + stage, 32 * (1 + MW), !live);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -1322,7 +1384,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<KIND, STAGES
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // the even CTA's MMAs no longer read or write this CTA
+    cluster_sync_all();  // every role is done; the odd CTA's fill count is in the even CTA
+    if (rank == 0 && threadIdx.x == 0)
+        drain_pair_loads<STAGES>(full, (int)fills[0], (int)fills[1], p.tx_a + p.tx_b + C_::SF_TX,
+                                 p.wait_limit_ns > kDrainLimitNs ? p.wait_limit_ns : kDrainLimitNs, err);
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves before every load of both has landed
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
