@@ -105,6 +105,34 @@ struct GemmParams {
     int32_t act_bf16;      // 1: bf16, 0: f32
 };
 
+// Waits that end a launch after an abort -- for loads and MMAs already
+// issued, which always complete -- use at least this limit, whatever limit
+// the caller set for the waits that can give up.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+
+// Named barrier `id` over `count` threads that also ORs a predicate across
+// them: returns whether any participant passed true (no shared-memory access).
+__device__ __forceinline__ bool named_bar_red_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Count `bytes` as arrived on the current phase of a barrier of this CTA.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// A 32-bit store into the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 template <int KIND, int BN, int STAGES, int SWAP, int NBUF_ = 0, int ACT_ATOMS = 0, int SA = 1>
 struct Cfg {
     // SA: K atoms (128 bytes of K per operand row) per pipeline stage; a stage
@@ -566,13 +594,16 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 }
             }
         }
-        if (!ok) {
-            // drain: wait (bounded) for our own loads still in flight
-            if (p.sf_rowmajor) cp_async_wait_all();
-            if (lane == 0)
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, p.wait_limit_ns, err);
-        }
+        // drain, on every path (another role may have given up on a stage whose
+        // load is still in flight; otherwise these waits return at once): every
+        // load this CTA issued lands before it may leave
+        if (p.sf_rowmajor) cp_async_wait_all();
+        if (lane == 0)
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait(&full[s], (issued_phase >> s) & 1u,
+                              p.wait_limit_ns > kDrainLimitNs ? p.wait_limit_ns : kDrainLimitNs, err);
+        __syncwarp();
     } else if (warp == 1 || (C_::MW > 1 && warp == C_::GATE_WARP + 1)) {
         // ---------------------------------------------------------- MMA issue
         // The whole warp walks the schedule and syncs on stage s's named
@@ -618,7 +649,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             }
             const uint32_t d_tmem = tmem + kAccCol + (acc * C_::MW + m) * BN;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                named_bar_sync(1 + stage, 32 * (1 + C_::MW));  // the gate saw this stage's data land
+                // the gate saw this stage's data land, or gave up waiting for it
+                if (named_bar_red_or(1 + stage, 32 * (1 + C_::MW), false)) live = false;
                 if (lane == 0 && live) {
                     tc_fence_after();
                     // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
@@ -702,7 +734,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         if (lane == 0) {
             // every tcgen05 op issued by this thread completes before TMEM is freed
             tc_commit(mma_done);
-            mbar_wait(mma_done, 0, p.wait_limit_ns, err);
+            mbar_wait(mma_done, 0, p.wait_limit_ns > kDrainLimitNs ? p.wait_limit_ns : kDrainLimitNs, err);
         }
         __syncwarp();
     } else if (warp == C_::GATE_WARP) {
@@ -726,7 +758,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                         if (lane == 0) *abort_flag = 1;
                     }
                 }
-                named_bar_sync(1 + stage, 32 * (1 + C_::MW));
+                // after a give-up the MMA warps issue nothing more, so a slot is
+                // released (and refilled) only once its data has landed
+                named_bar_red_or(1 + stage, 32 * (1 + C_::MW), !live);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -983,34 +1017,6 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
 // and scale tensor: the per-stage issue cost is paid once per SA atoms).
 // MMA-issuing warps of the two-atom pair configurations
 constexpr int kPairMW = 2;
-
-// Waits that end a launch after an abort -- for loads and MMAs already
-// issued, which always complete -- use at least this limit, whatever limit
-// the caller set for the waits that can give up.
-constexpr uint64_t kDrainLimitNs = 1000000000ull;
-
-// Named barrier `id` over `count` threads that also ORs a predicate across
-// them: returns whether any participant passed true (no shared-memory access).
-__device__ __forceinline__ bool named_bar_red_or(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-// Count `bytes` as arrived on the current phase of a barrier of this CTA.
-__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-// A 32-bit store into the shared memory of another CTA of the cluster.
-__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
 
 // After the pair kernel's loop, in the even CTA (one thread, after a cluster
 // barrier that made the odd CTA's fill count visible): every load either CTA

@@ -26,40 +26,44 @@ def test_wait_gives_up_and_reports_timeout():
     assert np.array_equal(codes.cpu().numpy().reshape(oc.shape), oc)
 
 
-# The pair GEMM's own bounded waits, made to run out: in a child process whose
-# wait limit is 1 us (the library reads MX_WAIT_LIMIT_NS once per process), a
-# 512 x 512 x 2048 E4M3 product takes the CTA-pair kernel with two-atom stages
-# and two MMA warps; its gate gives up on a stage that has not landed within
-# 1 us, the MMA warps stop issuing, the producers stop on their next slot wait,
-# and before the CTAs leave, the even CTA waits (with a limit of at least 1 s)
-# for every load either CTA issued and the MMA warps for every MMA.  The child
-# checks that the device error word reports the timeout and that the same
-# context then quantizes bit-exactly.
-_PAIR_ABORT_CHILD = r"""
+# The GEMM kernels' own bounded waits, made to run out: in a child process
+# whose wait limit is 1 us (the library reads MX_WAIT_LIMIT_NS once per
+# process) a product runs until the device error word reports a timeout, and
+# the same context must then quantize bit-exactly.  512 x 512 x 32768 E4M3 takes
+# the CTA-pair kernel (two-atom stages, two MMA warps), 16 x 8192 x 32768
+# E4M3 x E2M1 the one-CTA decode kernel (operands swapped, two MMA warps; K
+# long enough that each CTA's epilogue waits tens of microseconds, since a
+# wait looks at the clock only every 64 tries).  In
+# both, the gate gives up on a stage that has not landed within 1 us and the
+# MMA warps then issue nothing more, the producers stop on their next slot
+# wait, and before the CTAs leave every load either CTA of a pair issued has
+# landed and every MMA has completed (those waits use at least 1 s).
+_ABORT_CHILD = r"""
+import sys
 import numpy as np, torch
 import bit_gemm_gb300 as mx
 import oracle
-rng = np.random.default_rng(7)
-M = N = 512
-K = 2048
-A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).cuda()
-B = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32)).cuda()
-ac, as_ = mx.alloc_codes(M, K, mx.E4M3FN), mx.alloc_scales(M, K, mx.SCALES_MMA)
-bc, bs = mx.alloc_codes(N, K, mx.E4M3FN), mx.alloc_scales(N, K, mx.SCALES_MMA)
-mx.mx_quantize(A, mx.E4M3FN, ac, as_, mx.SCALES_MMA)
-mx.mx_quantize(B, mx.E4M3FN, bc, bs, mx.SCALES_MMA)
+M, N, K = (int(v) for v in sys.argv[1:4])
+fa, fb = int(sys.argv[4]), int(sys.argv[5])
+torch.manual_seed(7)
+A = torch.randn(M, K, device="cuda")
+B = torch.randn(N, K, device="cuda")
+ac, as_ = mx.alloc_codes(M, K, fa), mx.alloc_scales(M, K, mx.SCALES_MMA)
+bc, bs = mx.alloc_codes(N, K, fb), mx.alloc_scales(N, K, mx.SCALES_MMA)
+mx.mx_quantize(A, fa, ac, as_, mx.SCALES_MMA)
+mx.mx_quantize(B, fb, bc, bs, mx.SCALES_MMA)
 mx.mx_device_status()
 seen = 0
-for attempt in range(5):
+for attempt in range(20):
     C = torch.zeros(M, N, device="cuda")
-    mx.mx_block_matmul(ac, as_, mx.E4M3FN, bc, bs, mx.E4M3FN, M, N, K, C, mx.SCALES_MMA)
+    mx.mx_block_matmul(ac, as_, fa, bc, bs, fb, M, N, K, C, mx.SCALES_MMA)
     try:
         mx.mx_device_status()
     except mx.MxError as e:
         assert e.status == 5, e.status  # MX_ERR_TIMEOUT
         seen += 1
         break
-assert seen, "no wait of the pair kernel ran out within 1 us"
+assert seen, "no wait of the GEMM ran out within 1 us"
 mx.mx_device_status()  # the word was cleared
 x = torch.randn(64, 256, device="cuda")
 codes, scales = mx.alloc_codes(64, 256, mx.E4M3FN), mx.alloc_scales(64, 256)
@@ -68,18 +72,22 @@ mx.mx_device_status()
 oc, os_ = oracle.quantize(x.cpu().numpy(), oracle.E4M3)
 assert np.array_equal(codes.cpu().numpy().reshape(oc.shape), oc)
 assert np.array_equal(scales.cpu().numpy().reshape(os_.shape), os_)
-print("pair abort ok")
+print("abort ok")
 """
 
 
-def test_pair_gemm_waits_give_up_and_drain():
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (512, 512, 32768, mx.E4M3FN, mx.E4M3FN),  # CTA-pair kernel
+    (16, 8192, 32768, mx.E4M3FN, mx.E2M1),    # one-CTA decode kernel
+])
+def test_gemm_waits_give_up_and_drain(M, N, K, fa, fb):
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = dict(os.environ, MX_WAIT_LIMIT_NS="1000")
     env["PYTHONPATH"] = os.pathsep.join([root, os.path.join(root, "tests"), env.get("PYTHONPATH", "")])
-    r = subprocess.run([sys.executable, "-c", _PAIR_ABORT_CHILD], env=env, cwd=root, capture_output=True, text=True,
-                       timeout=600)
+    r = subprocess.run([sys.executable, "-c", _ABORT_CHILD, str(M), str(N), str(K), str(fa), str(fb)], env=env,
+                       cwd=root, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "pair abort ok" in r.stdout
+    assert "abort ok" in r.stdout
