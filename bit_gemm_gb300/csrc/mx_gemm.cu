@@ -313,6 +313,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned* err = &g_mx_device_error;
+    // fills the producer issued (fill n goes to slot n % STAGES), for the
+    // drain after the CTA's final barrier
+    int n_issued = 0;
     pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
@@ -501,13 +504,11 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         const uint32_t lbase = smem_u32(smem) + (li == 0 ? C_::OFF_A : li == 1 ? C_::OFF_B
                                                   : li == 2 ? C_::OFF_SFA : C_::OFF_SFB);
         const uint32_t lstep = li == 0 ? C_::A_BYTES : li == 1 ? C_::B_BYTES : li == 2 ? C_::SFA_BYTES : C_::SFB_BYTES;
-        uint32_t issued_mask = 0;  // stages whose latest load may still be in flight
         int fills = 0;
         // row-major scales: the lane's scale rows of the current tile, and their byte counts
         const uint8_t* rm_a[4];
         const uint8_t* rm_b[C_::SFB_TILES][4];
         uint32_t rm_na[4], rm_nb[C_::SFB_TILES][4];
-        uint32_t issued_phase = 0;
         bool ok = true;
         Work w;
         for (int it = 0; ok && work_at(it, w); ++it) {
@@ -519,8 +520,17 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // (the abort flag is consulted only when a bounded wait gives up:
                 // a shared-memory load and branch per stage would delay issue)
                 int okw = 1;
-                // (the first STAGES fills find their slots free: no wait)
-                if (lane == 0 && fills >= STAGES) okw = mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
+                // (the first STAGES fills find their slots free: no wait).  The
+                // slot's previous fill must also have landed: after the gate
+                // gives up, the MMA warps may release a slot whose load is still
+                // in flight, and a refill must not overlap it.  The parity is
+                // unambiguous because every earlier fill of the slot was seen
+                // landing here.  A fill lands before the MMAs release it, so
+                // this wait comes first and ends while the release is still
+                // pending: the refill is issued as soon as the release arrives.
+                if (lane == 0 && fills >= STAGES)
+                    okw = mbar_wait(&full[stage], phase ^ 1, p.wait_limit_ns, err) &&
+                          mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
                 ++fills;
                 okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
                 if (!okw) {
@@ -586,24 +596,15 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                     }
                     cp_async_arrive_noinc(&full[stage]);
                 }
-                issued_mask |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                ++n_issued;
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
         }
-        // drain, on every path (another role may have given up on a stage whose
-        // load is still in flight; otherwise these waits return at once): every
-        // load this CTA issued lands before it may leave
-        if (p.sf_rowmajor) cp_async_wait_all();
-        if (lane == 0)
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s))
-                    mbar_wait(&full[s], (issued_phase >> s) & 1u,
-                              p.wait_limit_ns > kDrainLimitNs ? p.wait_limit_ns : kDrainLimitNs, err);
-        __syncwarp();
+        // (loads still in flight after a give-up are awaited after the CTA's
+        // final barrier)
     } else if (warp == 1 || (C_::MW > 1 && warp == C_::GATE_WARP + 1)) {
         // ---------------------------------------------------------- MMA issue
         // The whole warp walks the schedule and syncs on stage s's named
@@ -650,7 +651,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
             const uint32_t d_tmem = tmem + kAccCol + (acc * C_::MW + m) * BN;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 // the gate saw this stage's data land, or gave up waiting for it
-                if (named_bar_red_or(1 + stage, 32 * (1 + C_::MW), false)) live = false;
+                // (the MMAs then read whatever the slot holds: the launch has
+                // reported its timeout, and the producer refills no slot whose
+                // load is in flight)
+                named_bar_sync(1 + stage, 32 * (1 + C_::MW));
                 if (lane == 0 && live) {
                     tc_fence_after();
                     // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
@@ -758,9 +762,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                         if (lane == 0) *abort_flag = 1;
                     }
                 }
-                // after a give-up the MMA warps issue nothing more, so a slot is
-                // released (and refilled) only once its data has landed
-                named_bar_red_or(1 + stage, 32 * (1 + C_::MW), !live);
+                named_bar_sync(1 + stage, 32 * (1 + C_::MW));
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -994,7 +996,24 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) {
+        tmem_dealloc(tmem, kTmemCols);
+    } else if (warp == 0 && *abort_flag) {
+        // Drain after a give-up (every give-up raises the flag before the
+        // barrier above; without one the gate saw every fill land): every
+        // load this CTA issued lands before it leaves.  Each slot's earlier
+        // fills were seen landing before its last one was issued, so the
+        // barrier is in that fill's phase.
+        if (p.sf_rowmajor) cp_async_wait_all();
+        if (lane == 0) {
+            const uint64_t lim = p.wait_limit_ns > kDrainLimitNs ? p.wait_limit_ns : kDrainLimitNs;
+            for (int s = 0; s < STAGES && s < n_issued; ++s) {
+                const int lf = s + ((n_issued - 1 - s) / STAGES) * STAGES;  // the slot's last fill
+                mbar_wait(&full[s], (uint32_t)(lf / STAGES) & 1u, lim, err);
+            }
+        }
+        __syncwarp();
+    }
 }
 
 // ------------------------------------------------------------ CTA pairs

@@ -29,15 +29,20 @@ def test_wait_gives_up_and_reports_timeout():
 # The GEMM kernels' own bounded waits, made to run out: in a child process
 # whose wait limit is 1 us (the library reads MX_WAIT_LIMIT_NS once per
 # process) a product runs until the device error word reports a timeout, and
-# the same context must then quantize bit-exactly.  512 x 512 x 32768 E4M3 takes
-# the CTA-pair kernel (two-atom stages, two MMA warps), 16 x 8192 x 32768
-# E4M3 x E2M1 the one-CTA decode kernel (operands swapped, two MMA warps; K
-# long enough that each CTA's epilogue waits tens of microseconds, since a
-# wait looks at the clock only every 64 tries).  In
-# both, the gate gives up on a stage that has not landed within 1 us and the
-# MMA warps then issue nothing more, the producers stop on their next slot
-# wait, and before the CTAs leave every load either CTA of a pair issued has
-# landed and every MMA has completed (those waits use at least 1 s).
+# the same context must then quantize bit-exactly.  The cases:
+#   512 x 512 x 32768 E4M3: the CTA-pair kernel (two-atom stages, two MMA
+#     warps).  After the gate gives up the MMA warps issue nothing more, and
+#     before the pair leaves every load either CTA issued has landed.
+#   16 x 8192 x 32768 E4M3 x E2M1: the one-CTA decode kernel (operands
+#     swapped, two MMA warps).  The producer refills a slot only once its
+#     previous load has landed, and after a give-up the CTA waits for its last
+#     loads before it leaves.
+# The kernel whose activation warps quantize into the ring is not driven
+# here: after a give-up an activation warp can arrive on a barrier phase it
+# does not own, so its drain is not certain.
+# K is long so that each CTA's waits last tens of microseconds: a wait looks
+# at the clock only every 64 tries.  The waits that end a launch (loads and
+# MMAs already issued) use at least 1 s.
 _ABORT_CHILD = r"""
 import sys
 import numpy as np, torch
