@@ -528,8 +528,11 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // landing here.  A fill lands before the MMAs release it, so
                 // this wait comes first and ends while the release is still
                 // pending: the refill is issued as soon as the release arrives.
+                // (Not with streamed activations: their warps' own arrivals
+                // on `full` already leave that kernel's drain uncertain after
+                // a give-up, and there the check lengthened the decode step.)
                 if (lane == 0 && fills >= STAGES)
-                    okw = mbar_wait(&full[stage], phase ^ 1, p.wait_limit_ns, err) &&
+                    okw = (C_::SACT || mbar_wait(&full[stage], phase ^ 1, p.wait_limit_ns, err)) &&
                           mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
                 ++fills;
                 okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
