@@ -300,7 +300,12 @@ MX_API mx_status_t mx_scales_relayout(const uint8_t* src, mx_scale_layout_t src_
 
 /* Synchronize `stream`, then report and clear the device-side error word
  * that kernels set when a bounded wait gives up (MX_ERR_TIMEOUT), or the
- * stream's CUDA error (MX_ERR_CUDA).  MX_OK when neither happened. */
+ * stream's CUDA error (MX_ERR_CUDA).  MX_OK when neither happened.  After a
+ * timeout the output of the launch that gave up is unspecified.  Before its
+ * CTAs exit, the GEMM waits at least 1 s for the loads and MMAs it already
+ * issued.  The one exception is the decode path of mx_block_matmul_act with
+ * bf16 activations and M <= 16, whose wait after a give-up is bounded but
+ * not certain to cover every load. */
 MX_API mx_status_t mx_device_status(void* stream);
 
 /* Failure-detection self test: launches one block that waits on a barrier
