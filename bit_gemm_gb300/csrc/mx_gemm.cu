@@ -613,8 +613,11 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
         // The whole warp walks the schedule and syncs on stage s's named
         // barrier (1 + s) with the gate warp, which has seen the stage's data
         // land; lane 0 issues.  MMA warp m (of MW) issues atoms
-        // [m SA / MW, (m + 1) SA / MW) of every stage into accumulator m.  After an abort the warp keeps walking (and
-        // syncing) without issuing, so its syncs and the gate's always pair up.
+        // [m SA / MW, (m + 1) SA / MW) of every stage into accumulator m.  The
+        // warp learns of an abort at its next tile (the abort flag, or its own
+        // wait giving up); until then it may issue on stages the gate gave up
+        // on.  After that it keeps walking (and syncing) without issuing, so
+        // its syncs and the gate's always pair up.
         // Everything that does not depend on the stage is built once: the
         // shared-memory descriptors of stage 0 (a stage's descriptors differ
         // only in the start-address field, which is advanced by adds) and the
