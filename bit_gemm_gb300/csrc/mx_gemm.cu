@@ -528,9 +528,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // landing here.  A fill lands before the MMAs release it, so
                 // this wait comes first and ends while the release is still
                 // pending: the refill is issued as soon as the release arrives.
-                // (Not with streamed activations: their warps' own arrivals
-                // on `full` already leave that kernel's drain uncertain after
-                // a give-up, and there the check lengthened the decode step.)
+                // (Not with streamed activations: there the MMA warps stop at
+                // the stage the gate gave up on, so no slot is released before
+                // its data has landed, and the check lengthened the decode step.)
                 if (lane == 0 && fills >= STAGES)
                     okw = (C_::SACT || mbar_wait(&full[stage], phase ^ 1, p.wait_limit_ns, err)) &&
                           mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, err);
@@ -659,8 +659,15 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                 // the gate saw this stage's data land, or gave up waiting for it
                 // (the MMAs then read whatever the slot holds: the launch has
                 // reported its timeout, and the producer refills no slot whose
-                // load is in flight)
-                named_bar_sync(1 + stage, 32 * (1 + C_::MW));
+                // load is in flight).  With streamed activations the warps stop
+                // at that stage instead: releasing later slots would let an
+                // activation warp run a phase ahead and arrive on a barrier
+                // phase not its own.
+                if constexpr (C_::SACT) {
+                    if (named_bar_red_or(1 + stage, 32 * (1 + C_::MW), false)) live = false;
+                } else {
+                    named_bar_sync(1 + stage, 32 * (1 + C_::MW));
+                }
                 if (lane == 0 && live) {
                     tc_fence_after();
                     // scales gathered with cp.async (generic proxy) are read by tcgen05.cp
@@ -768,7 +775,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, STAGES, SWAP, NBUF_, ACT_ATOMS, 
                         if (lane == 0) *abort_flag = 1;
                     }
                 }
-                named_bar_sync(1 + stage, 32 * (1 + C_::MW));
+                if constexpr (C_::SACT) named_bar_red_or(1 + stage, 32 * (1 + C_::MW), !live);
+                else named_bar_sync(1 + stage, 32 * (1 + C_::MW));
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;

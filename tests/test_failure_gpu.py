@@ -38,8 +38,8 @@ def test_wait_gives_up_and_reports_timeout():
 #     previous load has landed, and after a give-up the CTA waits for its last
 #     loads before it leaves.
 # The kernel whose activation warps quantize into the ring is not driven
-# here: after a give-up an activation warp can arrive on a barrier phase it
-# does not own, so its drain is not certain.
+# here: after a give-up its drain can wait for an activation warp's arrival
+# that never comes, and then it waits out its limit of at least 1 s.
 # K is long so that each CTA's waits last tens of microseconds: a wait looks
 # at the clock only every 64 tries.  The waits that end a launch (loads and
 # MMAs already issued) use at least 1 s.
